@@ -1,0 +1,206 @@
+/*
+ * pa.h -- C ABI of libpa.so: paged KV cache decode on one GB300 (sm_103a).
+ *
+ * Method sources (page title, section):
+ *   [PA] "論文解説: PagedAttention — 仮想メモリ着想のKVキャッシュ管理でLLMサービングを高効率化"
+ *   [VA] "論文解説: vAttention - PagedAttentionを使わないLLMサービング向け動的メモリ管理"
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every call returns a pa_status; nothing crosses the ABI as an exception.
+ *   On a non-OK status pa_last_error() holds a message (per calling thread).
+ * - Device calls take device pointers owned by the caller, enqueue work on
+ *   `stream` (a cudaStream_t; NULL = the legacy default stream) and return
+ *   without synchronising.  They allocate no device memory: scratch space is
+ *   a caller-provided workspace.  Pointers must be 16-byte aligned.
+ * - Out-of-range arguments that the host can see are rejected, never clamped
+ *   (the vAttention explainer's request-offset helper raises on an identifier
+ *   outside [0, max_batch); the same rule is applied throughout).
+ * - Indices that live in device memory (slots, block-table entries, context
+ *   lengths, request ids, copy pairs) are checked by the kernels: an offending
+ *   element is skipped, and when `dev_err` is non-NULL the kernel ORs a
+ *   PA_DEV_ERR_* bit into *dev_err (a device int the caller zeroes and reads
+ *   back).  No kernel traps, and no kernel waits without a time limit: a wait
+ *   that exceeds about one second sets PA_DEV_ERR_TIMEOUT and the kernel
+ *   returns.
+ *
+ * Data layout
+ * -----------
+ * KV pool: [NB][B][2][H_kv][D] elements of `kv_dtype`; index 0 on the third
+ * axis is K, 1 is V (the explainer's kv_cache of shape (blocks, B, 2, d),
+ * widened to H_kv heads).  Token position t of a sequence lives in logical
+ * block t / B at offset t % B; its slot is physical_block * B + t % B.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID = 1,     /* bad argument (shape, range, alignment, unknown id) */
+    PA_ERR_OOM = 2,         /* the block allocator has too few free blocks; state unchanged */
+    PA_ERR_STATE = 3,       /* the allocator's state forbids the operation (e.g. refcount underflow) */
+    PA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed; message in pa_last_error() */
+    PA_ERR_UNSUPPORTED = 5  /* valid but not built: dtype / head dim / block size / group size */
+} pa_status;
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2 } pa_dtype;
+
+/* Bits a kernel ORs into *dev_err. */
+#define PA_DEV_ERR_SLOT 0x1      /* slot_mapping entry >= NB*B */
+#define PA_DEV_ERR_BLOCK 0x2     /* block-table entry or copy pair outside [0, NB), or chained copy pairs */
+#define PA_DEV_ERR_CTX 0x4       /* context length < 1, > max_ctx or > MB*B */
+#define PA_DEV_ERR_REQ 0x8       /* request id outside [0, N_max) */
+#define PA_DEV_ERR_TIMEOUT 0x10  /* a bounded wait inside a kernel ran out */
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char* pa_last_error(void);
+
+/* Library version string. */
+const char* pa_version(void);
+
+/* Number of kernels this library has launched in this process (all threads). */
+uint64_t pa_launch_count(void);
+
+/* ------------------------------------------------------------------------
+ * Cache write ([PA] 技術的詳細 / PagedAttentionアルゴリズム: tokens are stored in
+ * fixed-size blocks reached through the block table; the slot encoding
+ * physical_block * B + offset is this library's).
+ * k, v: [T][H_kv][D] of dtype; pool: [NB][B][2][H_kv][D] of dtype;
+ * slot_mapping: [T] int64.  Token i's K and V rows are copied bit for bit to
+ * pool[slot / B][slot % B][0] and [1].  slot < 0 skips the token (padding);
+ * slot >= NB*B is skipped and flagged PA_DEV_ERR_SLOT.  Two tokens with the
+ * same slot race (caller error).  T == 0 is a no-op.
+ * Supported: dtype F16/BF16, (H_kv * D) a multiple of 8.
+ * ---------------------------------------------------------------------- */
+pa_status pa_reshape_and_cache(const void* k, const void* v, void* pool, const int64_t* slot_mapping, int T, int NB,
+                               int B, int H_kv, int D, pa_dtype dtype, int* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Copy-on-write block copy ([PA] 技術的詳細 / Copy-on-Write KVキャッシュ共有:
+ * a block shared by several sequences is copied before one of them writes).
+ * pairs: [n][2] int64 (src, dst), device memory.  pool[dst] = pool[src] for
+ * whole blocks (B * 2 * H_kv * D elements), bit for bit.  The pairs must not
+ * chain: destinations are distinct and no destination is also a source in the
+ * same call (flagged PA_DEV_ERR_BLOCK if violated; the copies then race).
+ * A pair with an index outside [0, NB) is skipped and flagged.  n == 0 is a no-op.
+ * ---------------------------------------------------------------------- */
+pa_status pa_copy_blocks(void* pool, const int64_t* pairs, int n, int NB, int B, int H_kv, int D, pa_dtype dtype,
+                         int* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Workspace for pa_decode / pa_decode_contiguous, in bytes.
+ * partition_tokens: 0 = default (512), -1 = one partition per sequence,
+ * > 0 = split each context into partitions of that many tokens (a multiple
+ * of 32).  max_ctx bounds every context length of the calls that use the
+ * workspace.  Returns 0 for invalid arguments.
+ * ---------------------------------------------------------------------- */
+size_t pa_decode_workspace_bytes(int N, int H_q, int H_kv, int D, int max_ctx, int partition_tokens);
+
+/* ------------------------------------------------------------------------
+ * Paged decode attention ([PA] 技術的詳細 / PagedAttentionアルゴリズム, decode
+ * equation; アルゴリズムの擬似コード for the block-by-block online softmax).
+ * For every sequence s < N and query head h < H_q, with g = h / (H_q / H_kv):
+ *     x_t = scale * (q[s][h] . K_t),  t = 0 .. ctx_lens[s]-1,
+ *     out[s][h] = sum_t softmax(x)_t * V_t,
+ * K_t, V_t = pool[block_tables[s][t / B]][t % B][0 / 1][g].
+ *
+ * out: [N][H_q][D] of out_dtype (F32, F16 or BF16); q: [N][H_q][D] of kv_dtype;
+ * block_tables: [N][MB] int32 (entries past ceil(ctx/B) are not read);
+ * ctx_lens: [N] int32 in [1, min(max_ctx, MB*B)];
+ * scale: usually 1/sqrt(D).
+ * Long contexts are split into partitions of partition_tokens (see
+ * pa_decode_workspace_bytes); partitions are merged by the same kernel that
+ * pa_partition_reduce runs.  workspace: ws_bytes >= pa_decode_workspace_bytes(...)
+ * of device memory, contents need not be initialised, and must not be used by
+ * another call that overlaps on the GPU.
+ * attend_events: NULL, or a pointer to two cudaEvent_t that are recorded on
+ * `stream` immediately before and after the attention kernel (for timing it
+ * apart from the scheduling and merge kernels).
+ * Supported: kv_dtype F16/BF16, D in {64, 128}, B in {4, 8, 16, 32},
+ * 1 <= H_q / H_kv <= 8, NB*B < 2^31.
+ * ---------------------------------------------------------------------- */
+pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* pool, const int32_t* block_tables,
+                    const int32_t* ctx_lens, int N, int H_q, int H_kv, int D, int B, int MB, int NB, int max_ctx,
+                    float scale, int partition_tokens, void* workspace, size_t ws_bytes, pa_dtype kv_dtype,
+                    int* dev_err, void* const* attend_events, void* stream);
+
+/* ------------------------------------------------------------------------
+ * The same attention over contiguous per-request buffers ([VA] 技術的詳細 /
+ * リクエスト単位のKVキャッシュインデキシング: request r's cache is the sub-tensor
+ * starting at r * S, S = max context * H_kv * D elements).
+ * k_buf, v_buf: [N_max][S_max][H_kv][D] of kv_dtype; req_ids: [N] int32 in
+ * [0, N_max) (out-of-range ids are flagged PA_DEV_ERR_REQ and their rows are
+ * not written); ctx_lens[s] <= S_max.  Other arguments as pa_decode.
+ * ---------------------------------------------------------------------- */
+pa_status pa_decode_contiguous(void* out, pa_dtype out_dtype, const void* q, const void* k_buf, const void* v_buf,
+                               const int32_t* req_ids, const int32_t* ctx_lens, int N, int H_q, int H_kv, int D,
+                               int N_max, int S_max, int max_ctx, float scale, int partition_tokens, void* workspace,
+                               size_t ws_bytes, pa_dtype kv_dtype, int* dev_err, void* const* attend_events,
+                               void* stream);
+
+/* ------------------------------------------------------------------------
+ * Merge of split-context partials (the running maximum / exponential sum /
+ * unnormalised output the block-by-block online softmax keeps, [PA]
+ * アルゴリズムの擬似コード, taken per partition and combined).
+ * Row r has nparts[r] in [1, P] partitions; part_m2, part_l: [R][P] fp32,
+ * part_acc: [R][P][D] fp32.  m2 is the partition's maximum score in base-2
+ * units (max_t x_t * log2 e); l = sum_t 2^(x_t log2 e - m2);
+ * acc = sum_t 2^(x_t log2 e - m2) V_t.
+ *     M = max_p m2_p,  out[r] = sum_p 2^(m2_p - M) acc_p / sum_p 2^(m2_p - M) l_p.
+ * out: [R][D] of out_dtype.  D in {64, 128}.  Rows with nparts outside
+ * [1, P] are not written and are flagged PA_DEV_ERR_CTX.
+ * ---------------------------------------------------------------------- */
+pa_status pa_partition_reduce(void* out, pa_dtype out_dtype, const float* part_m2, const float* part_l,
+                              const float* part_acc, const int32_t* nparts, int R, int P, int D, int* dev_err,
+                              void* stream);
+
+/* ------------------------------------------------------------------------
+ * Host block allocator ([PA] 技術的詳細 / PagedAttentionアルゴリズム and
+ * Copy-on-Write KVキャッシュ共有; 実装のポイント: one slab, the library's own
+ * allocator).  An opaque handle owned by the library; pa_alloc_destroy frees it.
+ * Not thread-safe: one thread per handle at a time.
+ * - Free list: a LIFO stack.  initial_free_order (nullable = 0..NB-1) lists
+ *   block ids in hand-out order.  Freeing pushes a sequence's blocks in
+ *   logical order.
+ * - Appending token position pos: if pos % B == 0 a free block is appended to
+ *   the table; otherwise, if the last block's reference count is above one, a
+ *   free block replaces it, (old, new) is emitted as a copy pair and the old
+ *   count drops by one (copy before write).  Slot = block * B + pos % B.
+ * - Every call is all-or-nothing: PA_ERR_OOM and PA_ERR_INVALID leave the
+ *   state unchanged.
+ * ---------------------------------------------------------------------- */
+pa_status pa_alloc_create(int NB, int B, const int32_t* initial_free_order, void** out);
+void pa_alloc_destroy(void* alloc);
+pa_status pa_alloc_add_seq(void* alloc, int seq_id);                 /* new empty sequence, seq_id >= 0 */
+/* Append n tokens to seq_id.  slots_out: [n]; cow_pairs_out: [cow_cap][2]
+ * (at most one pair per call); *n_cow receives the pair count. */
+pa_status pa_alloc_append_slots(void* alloc, int seq_id, int n, int64_t* slots_out, int64_t* cow_pairs_out,
+                                int cow_cap, int* n_cow);
+/* Append n_tokens[i] tokens to each of n_seqs distinct sequences, in order.
+ * slots_out: [sum n_tokens]; cow_pairs_out: [cow_cap][2]. */
+pa_status pa_alloc_append_batch(void* alloc, int n_seqs, const int32_t* seq_ids, const int32_t* n_tokens,
+                                int64_t* slots_out, int64_t* cow_pairs_out, int cow_cap, int* n_cow);
+pa_status pa_alloc_fork(void* alloc, int parent, int child);          /* child shares all parent blocks */
+pa_status pa_alloc_free_seq(void* alloc, int seq_id);                 /* drop references, recycle blocks */
+pa_status pa_alloc_block_table(void* alloc, int seq_id, int32_t* out, int cap, int* n);
+/* Pack the tables of n_seqs sequences into out[n_seqs][MB] (unused entries
+ * -1) and their lengths into ctx_out[n_seqs] (nullable). */
+pa_status pa_alloc_block_tables(void* alloc, int n_seqs, const int32_t* seq_ids, int32_t* out, int MB,
+                                int32_t* ctx_out);
+pa_status pa_alloc_seq_len(void* alloc, int seq_id, int64_t* out);
+pa_status pa_alloc_refcount(void* alloc, int block, int* out);
+int pa_alloc_num_free(void* alloc);                                   /* -1 for a NULL handle */
+pa_status pa_alloc_free_list(void* alloc, int32_t* out, int cap, int* n); /* next block to hand out first */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

@@ -1,0 +1,276 @@
+// alloc.cpp -- host block allocator behind pa_alloc_* (pa.h).
+//
+// PagedAttention explainer (0h-n0.github.io, arXiv 2309.06180):
+//  * 技術的詳細 / PagedAttentionアルゴリズム: a sequence of T tokens occupies
+//    ceil(T/B) blocks placed anywhere; a per-sequence table maps logical to
+//    physical blocks.
+//  * Copy-on-Write KVキャッシュ共有: shared blocks carry a reference count; a
+//    write into a block whose count is above one copies the block first.
+//  * 実装のポイント: one slab managed by the library's own allocator; blocks are
+//    taken on demand and returned when a request ends.
+// The free list is a LIFO stack; every call validates first and then applies,
+// so a failing call leaves the state unchanged.
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include "pa_internal.h"
+
+namespace pa {
+
+struct Seq {
+    std::vector<int32_t> blocks;
+    int64_t ntok = 0;
+};
+
+struct Allocator {
+    int NB = 0, B = 0;
+    std::vector<int32_t> free_stack;  // back() is handed out next
+    std::vector<int32_t> ref;
+    std::unordered_map<int, Seq> seqs;
+};
+
+static Allocator* as_alloc(void* h) { return static_cast<Allocator*>(h); }
+
+// Blocks a single-sequence append of n tokens takes from the free list, given
+// the current reference count `last_ref` of its last block.
+static int64_t blocks_needed(const Allocator& A, const Seq& s, int64_t n, int last_ref) {
+    if (n <= 0) return 0;
+    int64_t need = 0;
+    if (s.ntok % A.B != 0 && last_ref > 1) need += 1;  // copy-on-write of the shared partial block
+    const int64_t have = (s.ntok + A.B - 1) / A.B;
+    const int64_t want = (s.ntok + n + A.B - 1) / A.B;
+    return need + (want - have);
+}
+
+// Applies an append whose block demand has been checked.
+static void apply_append(Allocator& A, Seq& s, int64_t n, int64_t* slots, std::vector<int64_t>& cow) {
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t pos = s.ntok;
+        const int64_t off = pos % A.B;
+        if (off == 0) {
+            const int32_t b = A.free_stack.back();
+            A.free_stack.pop_back();
+            A.ref[b] = 1;
+            s.blocks.push_back(b);
+        } else if (A.ref[s.blocks.back()] > 1) {
+            const int32_t old = s.blocks.back();
+            const int32_t b = A.free_stack.back();
+            A.free_stack.pop_back();
+            A.ref[b] = 1;
+            A.ref[old] -= 1;
+            s.blocks.back() = b;
+            cow.push_back(old);
+            cow.push_back(b);
+        }
+        slots[i] = (int64_t)s.blocks[pos / A.B] * A.B + off;
+        s.ntok = pos + 1;
+    }
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+pa_status pa_alloc_create(int NB, int B, const int32_t* initial_free_order, void** out) {
+    if (!out) return fail(PA_ERR_INVALID, "out is null");
+    *out = nullptr;
+    if (NB <= 0 || B <= 0) return fail(PA_ERR_INVALID, "NB and B must be positive");
+    Allocator* A = new (std::nothrow) Allocator;
+    if (!A) return fail(PA_ERR_OOM, "host allocation failed");
+    A->NB = NB;
+    A->B = B;
+    A->ref.assign(NB, 0);
+    A->free_stack.resize(NB);
+    if (initial_free_order) {
+        std::vector<char> seen(NB, 0);
+        for (int i = 0; i < NB; ++i) {
+            const int32_t b = initial_free_order[i];
+            if (b < 0 || b >= NB || seen[b]) {
+                delete A;
+                return fail(PA_ERR_INVALID, "initial_free_order must be a permutation of 0..NB-1");
+            }
+            seen[b] = 1;
+            A->free_stack[NB - 1 - i] = b;
+        }
+    } else {
+        for (int i = 0; i < NB; ++i) A->free_stack[NB - 1 - i] = i;
+    }
+    *out = A;
+    return PA_OK;
+}
+
+void pa_alloc_destroy(void* alloc) { delete as_alloc(alloc); }
+
+pa_status pa_alloc_add_seq(void* alloc, int seq_id) {
+    Allocator* A = as_alloc(alloc);
+    if (!A) return fail(PA_ERR_INVALID, "null allocator");
+    if (seq_id < 0) return fail(PA_ERR_INVALID, "seq_id must be >= 0");
+    if (A->seqs.count(seq_id)) return fail(PA_ERR_INVALID, "sequence %d exists", seq_id);
+    A->seqs.emplace(seq_id, Seq());
+    return PA_OK;
+}
+
+pa_status pa_alloc_append_slots(void* alloc, int seq_id, int n, int64_t* slots_out, int64_t* cow_pairs_out,
+                                int cow_cap, int* n_cow) {
+    Allocator* A = as_alloc(alloc);
+    if (!A) return fail(PA_ERR_INVALID, "null allocator");
+    auto it = A->seqs.find(seq_id);
+    if (it == A->seqs.end()) return fail(PA_ERR_INVALID, "unknown sequence %d", seq_id);
+    if (n < 0) return fail(PA_ERR_INVALID, "negative token count");
+    if (n > 0 && !slots_out) return fail(PA_ERR_INVALID, "slots_out is null");
+    Seq& s = it->second;
+    const int last_ref = s.blocks.empty() ? 0 : A->ref[s.blocks.back()];
+    const int64_t need = blocks_needed(*A, s, n, last_ref);
+    const bool will_copy = n > 0 && s.ntok % A->B != 0 && last_ref > 1;
+    if (will_copy && (cow_cap < 1 || !cow_pairs_out)) return fail(PA_ERR_INVALID, "cow_pairs_out too small");
+    if (need > (int64_t)A->free_stack.size())
+        return fail(PA_ERR_OOM, "need %lld blocks, %zu free", (long long)need, A->free_stack.size());
+    std::vector<int64_t> cow;
+    apply_append(*A, s, n, slots_out, cow);
+    for (size_t i = 0; i < cow.size(); ++i) cow_pairs_out[i] = cow[i];
+    if (n_cow) *n_cow = (int)(cow.size() / 2);
+    return PA_OK;
+}
+
+pa_status pa_alloc_append_batch(void* alloc, int n_seqs, const int32_t* seq_ids, const int32_t* n_tokens,
+                                int64_t* slots_out, int64_t* cow_pairs_out, int cow_cap, int* n_cow) {
+    Allocator* A = as_alloc(alloc);
+    if (!A) return fail(PA_ERR_INVALID, "null allocator");
+    if (n_seqs < 0) return fail(PA_ERR_INVALID, "negative n_seqs");
+    if (n_seqs > 0 && (!seq_ids || !n_tokens)) return fail(PA_ERR_INVALID, "null argument");
+    // validate and count demand, following the reference counts the earlier
+    // sequences of the batch change
+    std::unordered_set<int> seen;
+    std::unordered_map<int32_t, int> ref_delta;
+    int64_t need = 0, total_tok = 0, copies = 0;
+    std::vector<Seq*> seqs(n_seqs);
+    for (int i = 0; i < n_seqs; ++i) {
+        auto it = A->seqs.find(seq_ids[i]);
+        if (it == A->seqs.end()) return fail(PA_ERR_INVALID, "unknown sequence %d", seq_ids[i]);
+        if (!seen.insert(seq_ids[i]).second) return fail(PA_ERR_INVALID, "sequence %d repeated", seq_ids[i]);
+        if (n_tokens[i] < 0) return fail(PA_ERR_INVALID, "negative token count");
+        Seq& s = it->second;
+        seqs[i] = &s;
+        int last_ref = 0;
+        if (!s.blocks.empty()) last_ref = A->ref[s.blocks.back()] + ref_delta[s.blocks.back()];
+        need += blocks_needed(*A, s, n_tokens[i], last_ref);
+        if (n_tokens[i] > 0 && s.ntok % A->B != 0 && last_ref > 1) {
+            ref_delta[s.blocks.back()] -= 1;
+            copies += 1;
+        }
+        total_tok += n_tokens[i];
+    }
+    if (total_tok > 0 && !slots_out) return fail(PA_ERR_INVALID, "slots_out is null");
+    if (copies > 0 && (cow_cap < copies || !cow_pairs_out)) return fail(PA_ERR_INVALID, "cow_pairs_out too small");
+    if (need > (int64_t)A->free_stack.size())
+        return fail(PA_ERR_OOM, "need %lld blocks, %zu free", (long long)need, A->free_stack.size());
+    std::vector<int64_t> cow;
+    int64_t off = 0;
+    for (int i = 0; i < n_seqs; ++i) {
+        apply_append(*A, *seqs[i], n_tokens[i], slots_out + off, cow);
+        off += n_tokens[i];
+    }
+    for (size_t i = 0; i < cow.size(); ++i) cow_pairs_out[i] = cow[i];
+    if (n_cow) *n_cow = (int)(cow.size() / 2);
+    return PA_OK;
+}
+
+pa_status pa_alloc_fork(void* alloc, int parent, int child) {
+    Allocator* A = as_alloc(alloc);
+    if (!A) return fail(PA_ERR_INVALID, "null allocator");
+    auto it = A->seqs.find(parent);
+    if (it == A->seqs.end()) return fail(PA_ERR_INVALID, "unknown sequence %d", parent);
+    if (child < 0 || A->seqs.count(child)) return fail(PA_ERR_INVALID, "child %d exists or is negative", child);
+    Seq c = it->second;
+    for (int32_t b : c.blocks) A->ref[b] += 1;
+    A->seqs.emplace(child, std::move(c));
+    return PA_OK;
+}
+
+pa_status pa_alloc_free_seq(void* alloc, int seq_id) {
+    Allocator* A = as_alloc(alloc);
+    if (!A) return fail(PA_ERR_INVALID, "null allocator");
+    auto it = A->seqs.find(seq_id);
+    if (it == A->seqs.end()) return fail(PA_ERR_INVALID, "unknown sequence %d", seq_id);
+    for (int32_t b : it->second.blocks)
+        if (A->ref[b] <= 0) return fail(PA_ERR_STATE, "block %d has no reference", b);
+    for (int32_t b : it->second.blocks) {
+        if (--A->ref[b] == 0) A->free_stack.push_back(b);
+    }
+    A->seqs.erase(it);
+    return PA_OK;
+}
+
+pa_status pa_alloc_block_table(void* alloc, int seq_id, int32_t* out, int cap, int* n) {
+    Allocator* A = as_alloc(alloc);
+    if (!A) return fail(PA_ERR_INVALID, "null allocator");
+    auto it = A->seqs.find(seq_id);
+    if (it == A->seqs.end()) return fail(PA_ERR_INVALID, "unknown sequence %d", seq_id);
+    const auto& bl = it->second.blocks;
+    if (n) *n = (int)bl.size();
+    if ((int)bl.size() > cap || (!out && !bl.empty())) return fail(PA_ERR_INVALID, "capacity %d < %zu", cap, bl.size());
+    if (!bl.empty()) std::memcpy(out, bl.data(), bl.size() * sizeof(int32_t));
+    return PA_OK;
+}
+
+pa_status pa_alloc_block_tables(void* alloc, int n_seqs, const int32_t* seq_ids, int32_t* out, int MB,
+                                int32_t* ctx_out) {
+    Allocator* A = as_alloc(alloc);
+    if (!A) return fail(PA_ERR_INVALID, "null allocator");
+    if (n_seqs < 0 || MB <= 0) return fail(PA_ERR_INVALID, "bad sizes");
+    if (n_seqs > 0 && (!seq_ids || !out)) return fail(PA_ERR_INVALID, "null argument");
+    for (int i = 0; i < n_seqs; ++i) {
+        auto it = A->seqs.find(seq_ids[i]);
+        if (it == A->seqs.end()) return fail(PA_ERR_INVALID, "unknown sequence %d", seq_ids[i]);
+        if ((int64_t)it->second.blocks.size() > MB)
+            return fail(PA_ERR_INVALID, "sequence %d has %zu blocks > MB %d", seq_ids[i], it->second.blocks.size(), MB);
+    }
+    for (int i = 0; i < n_seqs; ++i) {
+        const Seq& s = A->seqs.find(seq_ids[i])->second;
+        int32_t* row = out + (size_t)i * MB;
+        std::copy(s.blocks.begin(), s.blocks.end(), row);
+        std::fill(row + s.blocks.size(), row + MB, -1);
+        if (ctx_out) ctx_out[i] = (int32_t)s.ntok;
+    }
+    return PA_OK;
+}
+
+pa_status pa_alloc_seq_len(void* alloc, int seq_id, int64_t* out) {
+    Allocator* A = as_alloc(alloc);
+    if (!A || !out) return fail(PA_ERR_INVALID, "null argument");
+    auto it = A->seqs.find(seq_id);
+    if (it == A->seqs.end()) return fail(PA_ERR_INVALID, "unknown sequence %d", seq_id);
+    *out = it->second.ntok;
+    return PA_OK;
+}
+
+pa_status pa_alloc_refcount(void* alloc, int block, int* out) {
+    Allocator* A = as_alloc(alloc);
+    if (!A || !out) return fail(PA_ERR_INVALID, "null argument");
+    if (block < 0 || block >= A->NB) return fail(PA_ERR_INVALID, "block %d out of range", block);
+    *out = A->ref[block];
+    return PA_OK;
+}
+
+int pa_alloc_num_free(void* alloc) {
+    Allocator* A = as_alloc(alloc);
+    return A ? (int)A->free_stack.size() : -1;
+}
+
+pa_status pa_alloc_free_list(void* alloc, int32_t* out, int cap, int* n) {
+    Allocator* A = as_alloc(alloc);
+    if (!A) return fail(PA_ERR_INVALID, "null allocator");
+    const int sz = (int)A->free_stack.size();
+    if (n) *n = sz;
+    if (sz > cap || (!out && sz)) return fail(PA_ERR_INVALID, "capacity %d < %d", cap, sz);
+    for (int i = 0; i < sz; ++i) out[i] = A->free_stack[sz - 1 - i];
+    return PA_OK;
+}
+
+}  // extern "C"

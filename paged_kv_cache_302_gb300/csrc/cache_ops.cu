@@ -1,0 +1,106 @@
+// cache_ops.cu -- cache write through slot_mapping and copy-on-write block copy.
+//
+// Both are bit copies of 16-byte vectors; neither converts or interprets the
+// elements.  Sources: PagedAttention explainer (0h-n0.github.io, arXiv
+// 2309.06180), 技術的詳細 / PagedAttentionアルゴリズム (tokens stored in fixed-size
+// blocks reached through a block table) and Copy-on-Write KVキャッシュ共有 (copy a
+// shared block before writing into it).
+#include "pa_device.cuh"
+
+namespace pa {
+
+// One CTA per token (grid-stride).  Token i's K row and V row (H_kv*D elements
+// each, contiguous in both source and pool) are copied to slot slots[i].
+__global__ void __launch_bounds__(128) reshape_and_cache_kernel(const uint4* __restrict__ k,
+                                                                const uint4* __restrict__ v, uint4* __restrict__ pool,
+                                                                const int64_t* __restrict__ slots, int T,
+                                                                int64_t nslots, int row_vec, int B, int* err) {
+    for (int i = blockIdx.x; i < T; i += gridDim.x) {
+        const int64_t slot = slots[i];
+        if (slot < 0) continue;
+        if (slot >= nslots) {
+            if (threadIdx.x == 0) flag_error(err, PA_DEV_ERR_SLOT);
+            continue;
+        }
+        const int64_t blk = slot / B, off = slot - blk * B;
+        uint4* dk = pool + (blk * B + off) * 2 * (int64_t)row_vec;
+        uint4* dv = dk + row_vec;
+        const uint4* sk = k + (int64_t)i * row_vec;
+        const uint4* sv = v + (int64_t)i * row_vec;
+        for (int e = threadIdx.x; e < row_vec; e += blockDim.x) {
+            const uint4 a = sk[e];
+            const uint4 b = sv[e];
+            dk[e] = a;
+            dv[e] = b;
+        }
+    }
+}
+
+pa_status launch_reshape_and_cache(const void* k, const void* v, void* pool, const int64_t* slot_mapping, int T,
+                                   int NB, int B, int H_kv, int D, int* dev_err, cudaStream_t stream) {
+    if (T == 0) return PA_OK;
+    const int row_vec = H_kv * D * 2 / 16;
+    int grid = T < 152 * 16 ? T : 152 * 16;
+    reshape_and_cache_kernel<<<grid, 128, 0, stream>>>(static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+                                                       static_cast<uint4*>(pool), slot_mapping, T,
+                                                       (int64_t)NB * B, row_vec, B, dev_err);
+    count_launch();
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "reshape_and_cache launch");
+}
+
+// grid.x = pair index, grid.y = chunk of the block; each thread moves
+// kUnroll vectors per chunk with all loads issued before the stores.
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+
+__global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(uint4* __restrict__ pool,
+                                                                   const int64_t* __restrict__ pairs, int n, int NB,
+                                                                   int64_t blk_vec, int* err) {
+    const int i = blockIdx.x;
+    const int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+    if (src < 0 || src >= NB || dst < 0 || dst >= NB) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) flag_error(err, PA_DEV_ERR_BLOCK);
+        return;
+    }
+    if (blockIdx.y == 0) {
+        // chained pairs (a destination that is also a source, or a repeated
+        // destination) make the result order dependent: flag them
+        for (int j = threadIdx.x; j < n; j += blockDim.x) {
+            const int64_t sj = pairs[2 * j], dj = pairs[2 * j + 1];
+            if (sj == dst || (j != i && dj == dst)) flag_error(err, PA_DEV_ERR_BLOCK);
+        }
+    }
+    const uint4* s = pool + src * blk_vec;
+    uint4* d = pool + dst * blk_vec;
+    const int64_t chunk = (int64_t)kCopyThreads * kCopyUnroll;
+    for (int64_t base = (int64_t)blockIdx.y * chunk; base < blk_vec; base += (int64_t)gridDim.y * chunk) {
+        uint4 r[kCopyUnroll];
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+            const int64_t e = base + u * kCopyThreads + threadIdx.x;
+            if (e < blk_vec) r[u] = s[e];
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+            const int64_t e = base + u * kCopyThreads + threadIdx.x;
+            if (e < blk_vec) d[e] = r[u];
+        }
+    }
+}
+
+pa_status launch_copy_blocks(void* pool, const int64_t* pairs, int n, int NB, int B, int H_kv, int D, int* dev_err,
+                             cudaStream_t stream) {
+    if (n == 0) return PA_OK;
+    const int64_t blk_vec = (int64_t)B * 2 * H_kv * D * 2 / 16;
+    const int64_t chunk = (int64_t)kCopyThreads * kCopyUnroll;
+    int64_t gy = (blk_vec + chunk - 1) / chunk;
+    if (gy > 65535) gy = 65535;
+    dim3 grid(n, (unsigned)gy);
+    copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(static_cast<uint4*>(pool), pairs, n, NB, blk_vec, dev_err);
+    count_launch();
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "copy_blocks launch");
+}
+
+}  // namespace pa

@@ -1,0 +1,214 @@
+"""Host-side checks of libpa.so (no GPU): symbol exports, argument validation,
+and the C++ block allocator against the oracle's independent model."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import paged_kv_cache_302_gb300 as pa
+import workloads as W
+from oracle.alloc_model import AllocError, AllocModel
+
+
+def test_library_exports_every_declared_function():
+    L = pa.load()
+    names = pa.header_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(L, n), n
+    assert "sm_103a" in pa.version()
+
+
+def test_workspace_sizes():
+    assert pa.pa_decode_workspace_bytes(256, 32, 8, 128, 8192, 0) > 256 * 32 * 16 * 128 * 4
+    small = pa.pa_decode_workspace_bytes(4, 2, 2, 64, 33, -1)
+    assert 0 < small < 4096
+    for bad in [(0, 1, 1, 128, 10, 0), (1, 1, 1, 128, 10, 48), (1, 1, 1, 128, 0, 0)]:
+        with pytest.raises(pa.PAError):
+            pa.pa_decode_workspace_bytes(*bad)
+
+
+def test_device_calls_reject_bad_arguments_before_touching_the_gpu():
+    L = pa.load()
+    # unsupported dtype / bad sizes are refused by host validation
+    assert L.pa_reshape_and_cache(None, None, None, None, 1, 4, 4, 1, 8, 2, None, None) == pa.PA_ERR_UNSUPPORTED
+    assert L.pa_reshape_and_cache(None, None, None, None, -1, 4, 4, 1, 8, 1, None, None) == pa.PA_ERR_INVALID
+    assert L.pa_reshape_and_cache(None, None, None, None, 0, 4, 4, 1, 8, 1, None, None) == pa.PA_OK
+    assert L.pa_copy_blocks(None, None, 0, 4, 4, 1, 8, 1, None, None) == pa.PA_OK
+    assert L.pa_copy_blocks(None, None, 3, 4, 4, 1, 8, 1, None, None) == pa.PA_ERR_INVALID
+    st = L.pa_decode(None, 2, None, None, None, None, 1, 16, 1, 128, 16, 1, 1, 16, 0.1, 0, None, 0, 1, None, None,
+                     None)
+    assert st == pa.PA_ERR_UNSUPPORTED and "H_q / H_kv" in pa.last_error()
+    st = L.pa_decode(None, 2, None, None, None, None, 1, 2, 1, 96, 16, 1, 1, 16, 0.1, 0, None, 0, 1, None, None,
+                     None)
+    assert st == pa.PA_ERR_UNSUPPORTED
+    st = L.pa_decode(None, 0, None, None, None, None, 1, 2, 1, 128, 16, 1, 1, 16, 0.1, 0, None, 0, 1, None, None,
+                     None)
+    assert st == pa.PA_ERR_UNSUPPORTED and "out_dtype" in pa.last_error()
+    st = L.pa_partition_reduce(None, 2, None, None, None, None, 0, 4, 128, None, None)
+    assert st == pa.PA_OK
+
+
+def _run_same_ops(NB, B, order, ops):
+    """Apply the same operation list to the C++ allocator and the model; compare every observable."""
+    cpp = pa.BlockAllocator(NB, B, order)
+    ref = AllocModel(NB, B, order)
+    live = set()
+    for op in ops:
+        kind = op[0]
+        got_err = want_err = None
+        try:
+            if kind == "add":
+                cpp.add_seq(op[1])
+        except pa.PAError as e:
+            got_err = e.status
+        try:
+            if kind == "add":
+                ref.add_seq(op[1])
+        except AllocError as e:
+            want_err = e.kind
+        if kind == "append":
+            try:
+                got = cpp.append_slots(op[1], op[2])
+            except pa.PAError as e:
+                got_err, got = e.status, None
+            try:
+                want = ref.append_slots(op[1], op[2])
+            except AllocError as e:
+                want_err, want = e.kind, None
+            if got is not None and want is not None:
+                assert list(got[0]) == want[0]
+                assert [tuple(r) for r in got[1]] == want[1]
+        elif kind == "batch":
+            try:
+                got = cpp.append_batch(op[1], op[2])
+            except pa.PAError as e:
+                got_err, got = e.status, None
+            snapshot = (list(ref.free), list(ref.ref), {k: list(v) for k, v in ref.tables.items()}, dict(ref.ntok))
+            try:
+                slots, pairs = [], []
+                for s, n in zip(op[1], op[2]):
+                    a, b = ref.append_slots(s, n)
+                    slots += a
+                    pairs += b
+                want = (slots, pairs)
+            except AllocError as e:
+                want_err, want = e.kind, None
+                ref.free, ref.ref, ref.tables, ref.ntok = snapshot      # the batch is all-or-nothing
+            if got is not None and want is not None:
+                assert list(got[0]) == want[0]
+                assert [tuple(r) for r in got[1]] == want[1]
+        elif kind == "fork":
+            try:
+                cpp.fork(op[1], op[2])
+            except pa.PAError as e:
+                got_err = e.status
+            try:
+                ref.fork(op[1], op[2])
+            except AllocError as e:
+                want_err = e.kind
+        elif kind == "free":
+            try:
+                cpp.free_seq(op[1])
+            except pa.PAError as e:
+                got_err = e.status
+            try:
+                ref.free_seq(op[1])
+            except AllocError as e:
+                want_err = e.kind
+        kinds = {None: None, "invalid": pa.PA_ERR_INVALID, "oom": pa.PA_ERR_OOM, "state": pa.PA_ERR_STATE}
+        assert got_err == kinds[want_err], (op, got_err, want_err)
+        # full state comparison
+        assert cpp.num_free() == ref.num_free()
+        assert list(cpp.free_list()) == ref.free_list_top_first()
+        for s in ref.tables:
+            assert list(cpp.block_table(s)) == ref.block_table(s)
+            assert cpp.seq_len(s) == ref.seq_len(s)
+        for b in range(NB):
+            assert cpp.refcount(b) == ref.refcount(b)
+    cpp.close()
+
+
+def test_allocator_matches_model_on_worked_example():
+    w = W.tiny()
+    ops = [("add", s) for s in range(4)] + [("append", s, int(w.ctx[s])) for s in range(4)]
+    _run_same_ops(w.NB, w.B, w.free_order, ops)
+    a = pa.BlockAllocator(w.NB, w.B, w.free_order)
+    for s in range(4):
+        a.add_seq(s)
+        a.append_slots(s, int(w.ctx[s]))
+    assert list(a.block_table(0)) == [7, 1] and list(a.block_table(1)) == [3, 5]
+
+
+def test_allocator_matches_model_on_random_operations():
+    rng = np.random.default_rng(50)
+    for trial in range(12):
+        NB = int(rng.integers(6, 60))
+        B = int(rng.choice([1, 2, 4, 8, 16]))
+        ops, nxt, live = [], 0, []
+        for _ in range(150):
+            r = rng.integers(0, 10)
+            if r < 2 or not live:
+                ops.append(("add", nxt))
+                live.append(nxt)
+                nxt += 1
+            elif r < 5:
+                ops.append(("append", int(rng.choice(live + [999])), int(rng.integers(-1, 3 * B + 2))))
+            elif r < 7:
+                k = int(rng.integers(1, len(live) + 1))
+                ids = [int(x) for x in rng.choice(live, size=k, replace=False)]
+                ops.append(("batch", ids, [int(x) for x in rng.integers(0, 2 * B + 2, size=k)]))
+            elif r < 8:
+                ops.append(("fork", int(rng.choice(live)), nxt))
+                live.append(nxt)
+                nxt += 1
+            else:
+                s = int(rng.choice(live))
+                live.remove(s)
+                ops.append(("free", s))
+        ops = [o for o in ops if not (o[0] == "append" and o[2] < 0)]
+        _run_same_ops(NB, B, rng.permutation(NB), ops)
+
+
+def test_allocator_cow_workload_matches_model():
+    w = W.cow(prompts=3, samples=8, prompt_len=1030)
+    ops = []
+    for p in range(w.prompts):
+        base = p * w.samples
+        ops += [("add", base), ("append", base, w.prompt_len)]
+        ops += [("fork", base, base + j) for j in range(1, w.samples)]
+    ops.append(("batch", list(range(w.N)), [int(x) for x in w.extra]))
+    _run_same_ops(w.NB, w.B, w.free_order, ops)
+
+
+def test_allocator_errors():
+    a = pa.BlockAllocator(2, 4)
+    with pytest.raises(pa.PAError) as e:
+        a.append_slots(0, 1)
+    assert e.value.status == pa.PA_ERR_INVALID
+    a.add_seq(0)
+    with pytest.raises(pa.PAError) as e:
+        a.append_slots(0, 9)
+    assert e.value.status == pa.PA_ERR_OOM and a.num_free() == 2 and a.seq_len(0) == 0
+    with pytest.raises(pa.PAError):
+        a.append_batch([0, 0], [1, 1])
+    with pytest.raises(pa.PAError):
+        pa.BlockAllocator(3, 4, [0, 0, 1])
+    L = pa.load()
+    assert L.pa_alloc_num_free(None) == -1
+    h = ctypes.c_void_p()
+    assert L.pa_alloc_create(0, 4, None, ctypes.byref(h)) == pa.PA_ERR_INVALID
+
+
+def test_block_tables_packing():
+    a = pa.BlockAllocator(16, 4, list(range(16)))
+    for s, n in [(0, 5), (1, 9), (2, 1)]:
+        a.add_seq(s)
+        a.append_slots(s, n)
+    tab, ctx = a.block_tables([2, 0, 1], 4)
+    assert list(ctx) == [1, 5, 9]
+    assert list(tab[0]) == [5, -1, -1, -1]
+    assert list(tab[1]) == [0, 1, -1, -1]
+    assert list(tab[2]) == [2, 3, 4, -1]
+    with pytest.raises(pa.PAError):
+        a.block_tables([1], 2)

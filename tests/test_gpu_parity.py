@@ -1,0 +1,240 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Bit-exact: cache writes, block copies, allocator tables and slots.
+Attention outputs (fp32): max |diff| <= 2e-3 and relative L2 <= 1e-3.
+Small cases compare every output; full-size workloads compare a sample of
+(sequence, query head) rows the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import _cases as C
+import oracle
+import paged_kv_cache_302_gb300 as pa
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+# ----------------------------------------------------------------------------- cache ops
+
+def test_reshape_and_cache_bit_exact_skips_padding_and_flags_bad_slots():
+    w = W.llama3_8b(n_seqs=4)
+    rng = np.random.default_rng(1)
+    NB, B = 40, 16
+    pool = torch.zeros((NB, B, 2, w.H_kv, w.D), dtype=torch.bfloat16, device="cuda")
+    host = np.zeros(pool.shape, dtype=np.uint16)
+    T = 300
+    slots = rng.choice(NB * B, size=T, replace=False).astype(np.int64)
+    slots[[5, 17, 200]] = -1
+    k, v = W.token_kv(w, T)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_reshape_and_cache(C.to_dev(k, "bf16"), C.to_dev(v, "bf16"), pool, torch.from_numpy(slots).cuda(),
+                            dev_err=err)
+    oracle.reshape_and_cache(k, v, host, slots)
+    torch.cuda.synchronize()
+    assert np.array_equal(C.to_bits(pool), host) and err.item() == 0
+    bad = slots.copy()
+    bad[3] = NB * B
+    before = C.to_bits(pool)
+    pa.pa_reshape_and_cache(C.to_dev(k, "bf16"), C.to_dev(v, "bf16"), pool, torch.from_numpy(bad).cuda(),
+                            dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() & pa.PA_DEV_ERR_SLOT
+    assert np.array_equal(C.to_bits(pool), before)   # same data rewritten, bad slot skipped
+
+
+def test_copy_blocks_bit_exact_and_flags():
+    rng = np.random.default_rng(2)
+    NB, B, H, D = 30, 16, 8, 128
+    bits = W.normal_bits(rng, (NB, B, 2, H, D), "f16")
+    pool = C.to_dev(bits, "f16").clone()
+    pairs = np.array([[1, 20], [4, 21], [1, 22], [9, 0]], dtype=np.int64)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_copy_blocks(pool, torch.from_numpy(pairs).cuda(), dev_err=err)
+    oracle.copy_blocks(bits, pairs)
+    torch.cuda.synchronize()
+    assert np.array_equal(C.to_bits(pool), bits) and err.item() == 0
+    pa.pa_copy_blocks(pool, torch.from_numpy(np.array([[2, 3], [3, 5]], dtype=np.int64)).cuda(), dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() & pa.PA_DEV_ERR_BLOCK
+    err.zero_()
+    pa.pa_copy_blocks(pool, torch.from_numpy(np.array([[2, NB]], dtype=np.int64)).cuda(), dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() & pa.PA_DEV_ERR_BLOCK
+
+
+# ----------------------------------------------------------------------------- decode, every output
+
+def test_tiny_worked_example_every_output():
+    w = W.tiny()
+    c = C.build_paged(w)
+    assert list(c.tables[0][:2]) == [7, 1] and list(c.tables[1][:2]) == [3, 5]
+    ref = C.oracle_decode(c)
+    for pt in (0, -1, 32):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = C.gpu_decode(c, partition_tokens=pt, dev_err=err).cpu().numpy()
+        C.assert_close(out, ref, f"tiny pt={pt}")
+        assert err.item() == 0
+
+
+@pytest.mark.parametrize("pt", [0, -1, 32, 96])
+def test_llama_shaped_small_every_output(pt):
+    w = W.llama3_8b(n_seqs=24)
+    c = C.build_paged(w)
+    ref = C.oracle_decode(c)
+    out = C.gpu_decode(c, partition_tokens=pt).cpu().numpy()
+    C.assert_close(out, ref, f"llama small pt={pt}")
+
+
+def test_opt13b_shaped_small_every_output():
+    w = W.opt13b(n_seqs=6)
+    c = C.build_paged(w)
+    ref = C.oracle_decode(c)
+    out = C.gpu_decode(c).cpu().numpy()
+    C.assert_close(out, ref, "opt13b small")
+
+
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_yi34b_shaped_block_sizes_every_output(B):
+    w = W.yi34b_long(n_seqs=2, ctx_len=1500 + B, B=B)
+    c = C.build_paged(w)
+    ref = C.oracle_decode(c)
+    for pt in (0, -1):
+        out = C.gpu_decode(c, partition_tokens=pt).cpu().numpy()
+        C.assert_close(out, ref, f"yi34b B={B} pt={pt}")
+
+
+def test_ragged_lengths_cover_every_tail():
+    # contexts 1..70 exercise empty / partial 16-token tiles and partial stages
+    base = W.llama3_8b(n_seqs=70)
+    base.ctx = np.arange(1, 71, dtype=np.int32)
+    c = C.build_paged(base)
+    ref = C.oracle_decode(c)
+    for pt in (-1, 32):
+        out = C.gpu_decode(c, partition_tokens=pt).cpu().numpy()
+        C.assert_close(out, ref, f"ragged pt={pt}")
+
+
+def test_block_relabelling_gives_identical_bits():
+    w = W.llama3_8b(n_seqs=12)
+    c = C.build_paged(w, check_pool=False)
+    out1 = C.gpu_decode(c).cpu()
+    perm = np.random.default_rng(3).permutation(w.NB)
+    pool2 = torch.empty_like(c.pool)
+    pool2[torch.from_numpy(perm).cuda()] = c.pool
+    tables2 = np.where(c.tables >= 0, perm[np.maximum(c.tables, 0)], -1).astype(np.int32)
+    c2 = C.Paged(w, pool2, None, tables2, c.ctx, c.q)
+    out2 = C.gpu_decode(c2).cpu()
+    assert torch.equal(out1, out2)
+
+
+def test_contiguous_layout_matches_paged_bit_for_bit_and_oracle():
+    w = W.yi34b_long(n_seqs=3, ctx_len=2000, B=16)
+    w.ctx = np.array([2000, 1333, 77], dtype=np.int32)
+    c = C.build_paged(w)
+    N_max, S_max = 5, 2048
+    req = np.array([3, 0, 4], dtype=np.int32)
+    kb = torch.zeros((N_max, S_max, w.H_kv, w.D), dtype=torch.bfloat16, device="cuda")
+    vb = torch.zeros_like(kb)
+    kb.view(torch.int16).fill_(C.nan16("bf16"))
+    vb.view(torch.int16).fill_(C.nan16("bf16"))
+    hk = np.full(kb.shape, W.NAN_BITS["bf16"], dtype=np.uint16)
+    hv = hk.copy()
+    for s in range(w.N):
+        t = np.arange(int(w.ctx[s]))
+        phys = c.tables[s, t // w.B]
+        hk[req[s], : len(t)] = c.host_pool[phys, t % w.B, 0]
+        hv[req[s], : len(t)] = c.host_pool[phys, t % w.B, 1]
+    kb.copy_(C.to_dev(hk, "bf16"))
+    vb.copy_(C.to_dev(hv, "bf16"))
+    ref = oracle.contiguous_decode(c.q, hk, hv, req, w.ctx, "bf16")
+    for pt in (0, -1):
+        paged = C.gpu_decode(c, partition_tokens=pt)
+        out = torch.full_like(paged, float("nan"))
+        pa.pa_decode_contiguous(out, C.to_dev(c.q, "bf16"), kb, vb, torch.from_numpy(req).cuda(),
+                                torch.from_numpy(w.ctx).cuda(), int(w.ctx.max()), partition_tokens=pt)
+        torch.cuda.synchronize()
+        assert torch.equal(out, paged)
+        C.assert_close(out.cpu().numpy(), ref, f"contiguous pt={pt}")
+
+
+def test_low_precision_output_within_one_ulp_of_rounded_oracle():
+    w = W.llama3_8b(n_seqs=10)
+    c = C.build_paged(w)
+    ref = C.oracle_decode(c)
+    out = C.gpu_decode(c, out_dtype=torch.bfloat16).float().cpu().numpy()
+    ref_r = W.bits_to_float(W.round_bits(ref.astype(np.float32), "bf16"), "bf16").astype(np.float64)
+    ulp = np.abs(W.bits_to_float(W.round_bits(ref.astype(np.float32), "bf16") + 1, "bf16") - ref_r)
+    assert np.all(np.abs(out - ref_r) <= ulp * 1.001)
+
+
+def test_partition_reduce_standalone_matches_oracle_merge():
+    rng = np.random.default_rng(4)
+    R, P, D = 37, 9, 128
+    m2 = (rng.normal(size=(R, P)) * 3).astype(np.float32)
+    l = rng.uniform(0.5, 40.0, size=(R, P)).astype(np.float32)
+    acc = rng.normal(size=(R, P, D)).astype(np.float32)
+    nparts = rng.integers(1, P + 1, size=R).astype(np.int32)
+    ref = oracle.partition_merge(m2.astype(np.float64), l.astype(np.float64), acc.astype(np.float64), nparts)
+    out = torch.full((R, D), float("nan"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_partition_reduce(out, torch.from_numpy(m2).cuda(), torch.from_numpy(l).cuda(),
+                           torch.from_numpy(acc).cuda(), torch.from_numpy(nparts).cuda(), dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=2e-5, atol=2e-5)
+
+
+def test_device_errors_are_flagged_not_faulted():
+    w = W.llama3_8b(n_seqs=6)
+    c = C.build_paged(w)
+    tab, ctx = c.dev_tables()
+    qd = C.to_dev(c.q, w.dtype)
+    out = torch.zeros((w.N, w.H_q, w.D), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bad_ctx = ctx.clone()
+    bad_ctx[2] = 0
+    pa.pa_decode(out, qd, c.pool, tab, bad_ctx, int(c.ctx.max()), dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() & pa.PA_DEV_ERR_CTX
+    err.zero_()
+    bad_tab = tab.clone()
+    bad_tab[1, 0] = w.NB + 5
+    pa.pa_decode(out, qd, c.pool, bad_tab, ctx, int(c.ctx.max()), dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() & pa.PA_DEV_ERR_BLOCK
+    # the context is still usable afterwards
+    out2 = C.gpu_decode(c).cpu().numpy()
+    C.assert_close(out2, C.oracle_decode(c), "after flagged calls")
+
+
+# ----------------------------------------------------------------------------- full-size workloads, sampled rows
+
+def _full_check(c, pts=(0,), n_pairs=48):
+    pairs = C.sample_pairs(c.w, n_pairs)
+    ref = C.oracle_decode(c, pairs=pairs)
+    for pt in pts:
+        out = C.gpu_decode(c, partition_tokens=pt).cpu().numpy()
+        assert np.all(np.isfinite(out)), "every row is written"
+        C.assert_close(out[pairs[:, 0], pairs[:, 1]], ref[pairs[:, 0], pairs[:, 1]], f"{c.w.name} pt={pt}")
+
+
+def test_full_opt13b():
+    _full_check(C.build_paged(W.opt13b()), pts=(0, -1))
+
+
+def test_full_llama3_8b():
+    _full_check(C.build_paged(W.llama3_8b()), pts=(0, -1))
+
+
+def test_full_cow_parallel_sampling():
+    c, npairs = C.build_cow(W.cow())
+    assert npairs == 224
+    _full_check(c)
+
+
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_full_yi34b_long_context(B):
+    _full_check(C.build_paged(W.yi34b_long(B=B), check_pool=(B == 16)), n_pairs=16)
