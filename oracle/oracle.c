@@ -167,8 +167,10 @@ static const uint16_t* fetch_row(const kv_source* src, int s, int t, int g, int 
     }
 }
 
+/* out receives the row only at the end; it is never used as an accumulator, so a row listed
+ * twice and computed by two threads at once still ends up with the right values. */
 static int attend_one(double* out, const uint16_t* q, const kv_source* src, int s, int h, int n, int G, double scale,
-                      int dtype, double* x) {
+                      int dtype, double* x, double* acc) {
     const int D = src->D, g = h / G;
     /* pass 1: scores and their maximum */
     double m = -INFINITY;
@@ -186,13 +188,14 @@ static int attend_one(double* out, const uint16_t* q, const kv_source* src, int 
         x[t] = exp(x[t] - m);
         z += x[t];
     }
-    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (int d = 0; d < D; ++d) acc[d] = 0.0;
     for (int t = 0; t < n; ++t) {
         const uint16_t* vr = fetch_row(src, s, t, g, 1);
         if (!vr) return ORC_INVALID;
         double w = x[t] / z;
-        for (int d = 0; d < D; ++d) out[d] += w * widen(vr[d], dtype);
+        for (int d = 0; d < D; ++d) acc[d] += w * widen(vr[d], dtype);
     }
+    for (int d = 0; d < D; ++d) out[d] = acc[d];
     return ORC_OK;
 }
 
@@ -212,7 +215,7 @@ static int attend_rows(double* out, const uint16_t* q, const kv_source* src, con
 #pragma omp parallel num_threads(nthreads)
 #endif
     {
-        double* x = (double*)malloc(sizeof(double) * (size_t)(max_n > 0 ? max_n : 1));
+        double* x = (double*)malloc(sizeof(double) * (size_t)((max_n > 0 ? max_n : 1) + D));
         if (!x) {
 #ifdef _OPENMP
 #pragma omp atomic write
@@ -234,7 +237,7 @@ static int attend_rows(double* out, const uint16_t* q, const kv_source* src, con
                 int rc = ORC_INVALID;
                 if (s >= 0 && s < N && h >= 0 && h < H_q)
                     rc = attend_one(out + ((int64_t)s * H_q + h) * D, q + ((int64_t)s * H_q + h) * D, src, s, h, ctx[s], G,
-                                    scale, dtype, x);
+                                    scale, dtype, x, x + (max_n > 0 ? max_n : 1));
                 if (rc != ORC_OK) {
 #ifdef _OPENMP
 #pragma omp atomic write

@@ -159,7 +159,9 @@ def sample_pairs(w: W.Workload, n: int, seed: int = 0) -> np.ndarray:
     seqs = list(order[:2]) + list(order[-2:]) + list(rng.integers(0, w.N, size=max(0, n - 4)))
     heads = rng.integers(0, w.H_q, size=len(seqs))
     heads[: min(4, len(heads))] = [0, w.H_q - 1, w.G - 1 if w.G > 1 else 0, w.H_q // 2][: min(4, len(heads))]
-    return np.stack([np.asarray(seqs), heads], axis=1).astype(np.int32)
+    pairs = np.stack([np.asarray(seqs), heads], axis=1).astype(np.int32)
+    _, first = np.unique(pairs, axis=0, return_index=True)
+    return pairs[np.sort(first)]
 
 
 def assert_close(got: np.ndarray, want: np.ndarray, what: str = ""):

@@ -337,3 +337,13 @@ def test_copy_blocks_rejects_chained_duplicate_or_out_of_range(pairs):
     pool = W.normal_bits(rng, (10, 4, 2, 1, 16), "bf16")
     with pytest.raises(oracle.OracleError):
         oracle.copy_blocks(pool, np.array(pairs, dtype=np.int64))
+
+
+def test_rows_listed_twice_are_computed_correctly_in_parallel():
+    rng = np.random.default_rng(26)
+    q, pool, tables, ctx = _tiny_paged(rng, N=2, H_q=2, H_kv=1, D=16, ctx=(37, 29))
+    full = oracle.paged_decode(q, pool, tables, ctx, "bf16")
+    pairs = np.array([[0, 1]] * 16 + [[1, 0]] * 16, dtype=np.int32)
+    for _ in range(5):
+        sub = oracle.paged_decode(q, pool, tables, ctx, "bf16", pairs=pairs, nthreads=8)
+        assert np.array_equal(sub[0, 1], full[0, 1]) and np.array_equal(sub[1, 0], full[1, 0])
