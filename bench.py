@@ -1,0 +1,445 @@
+"""Benchmark: paged decode on the Llama-3-8B-shaped GQA workload.
+
+One step = one decode step of the whole hot path for 256 sequences:
+  host block allocation of the step's new token (done before the timed region
+  for the device-resident figure, inside it for the end-to-end figure),
+  copy-on-write block copies (none arise in this workload),
+  pa_reshape_and_cache of the new K/V, pa_decode (schedule, attention,
+  partition merge).
+Inputs: 256 sequences, lengths lognormal (median 1000, sigma 1.0, cap 8192),
+32 query / 8 KV heads, D 128, B 16, bf16 N(0,1), shuffled physical blocks
+(~1.65 GB of K/V per step: larger than L2, so no flush is needed).
+
+Output: one JSON line (rank 0).  `value` is KV-read GB/s over whole steps;
+`roofline` is the attention kernel alone against the measured HBM copy rate;
+`cpu_baseline` / `--impl reference` time the fp64 oracle on host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode KV-read GB/s (% of HBM peak), seq-steps/s at Llama-3-8B GQA"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attend_llama3_8b.json")
+DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_302_gb300", "csrc", "decode.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--partition-tokens", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def workload(steps: int, warmup: int) -> W.Workload:
+    # room for every decode step of the device and end-to-end phases
+    return W.llama3_8b(grow=2 * (steps + warmup) + 16)
+
+
+def config_dict(w: W.Workload, pt: int) -> dict:
+    return {
+        "workload": "llama3_8b_gqa_paged_decode",
+        "seqs": w.N, "H_q": w.H_q, "H_kv": w.H_kv, "D": w.D, "block_size": w.B, "kv_dtype": w.dtype,
+        "ctx": "lognormal(median 1000, sigma 1.0), capped at 8192",
+        "ctx_tokens_first_step": int(w.ctx.sum()),
+        "partition_tokens": 512 if pt == 0 else pt,
+        "l2": "inputs larger than L2 (about 1.65 GB of K/V per step), no flush",
+    }
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def oracle_sample_rate(w: W.Workload, host_pool, tables, ctx, q, target_s: float):
+    """Time the oracle over whole sequences (every query head) until ~target_s of CPU work."""
+    import oracle
+
+    order = np.random.default_rng(9).permutation(w.N)
+    nthreads = oracle.num_threads()
+    done_bytes, t_total, seqs = 0, 0.0, 0
+    per_tok = 2 * w.H_kv * w.D * w.elem_bytes
+    for chunk in np.array_split(order, 16):
+        pairs = np.array([(s, h) for s in chunk for h in range(w.H_q)], dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.paged_decode(q, host_pool, tables, ctx, w.dtype, pairs=pairs, nthreads=nthreads)
+        t_total += time.perf_counter() - t0
+        done_bytes += int(ctx[chunk].astype(np.int64).sum()) * per_tok
+        seqs += len(chunk)
+        if t_total * nthreads >= target_s or t_total >= target_s:
+            break
+    return done_bytes / t_total / 1e9, nthreads, seqs, t_total
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+
+    w = workload(args.steps, args.warmup)
+    host_pool, tables, ctx, slots = host_state(w)
+    q = W.queries(w)
+    nthreads = oracle.num_threads()
+    per_tok = 2 * w.H_kv * w.D * w.elem_bytes
+    # each step: the oracle over a fixed seeded subset of whole sequences
+    rng = np.random.default_rng(11)
+    subset = np.sort(rng.choice(w.N, size=8, replace=False))
+    pairs = np.array([(s, h) for s in subset for h in range(w.H_q)], dtype=np.int32)
+    step_bytes = int(ctx[subset].astype(np.int64).sum()) * per_tok
+    for _ in range(args.warmup):
+        oracle.paged_decode(q, host_pool, tables, ctx, w.dtype, pairs=pairs, nthreads=nthreads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.paged_decode(q, host_pool, tables, ctx, w.dtype, pairs=pairs, nthreads=nthreads)
+        times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    value = step_bytes / t / 1e9
+    sample = (f"fp64 oracle over all {w.H_q} query heads of 8 seeded sequences "
+              f"({int(ctx[subset].sum())} context tokens) per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w, args.partition_tokens),
+        "seq_steps_per_s": len(subset) / t,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nthreads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- shared setup
+
+def host_state(w: W.Workload):
+    """Host-side pool, tables and lengths of the workload (oracle layout), used by the CPU legs."""
+    import oracle
+    from oracle.alloc_model import AllocModel
+
+    m = AllocModel(w.NB, w.B, w.free_order)
+    slots = []
+    for s in range(w.N):
+        m.add_seq(s)
+        slots += m.append_slots(s, int(w.ctx[s]))[0]
+    slots = np.asarray(slots, dtype=np.int64)
+    MB = w.max_blocks_per_seq()
+    tables = np.full((w.N, MB), -1, dtype=np.int32)
+    for s in range(w.N):
+        t = m.block_table(s)
+        tables[s, : len(t)] = t
+    k, v = W.token_kv(w, slots.size)
+    pool = np.zeros((w.NB, w.B, 2, w.H_kv, w.D), dtype=np.uint16)
+    oracle.reshape_and_cache(k, v, pool, slots)
+    return pool, tables, w.ctx.copy(), slots
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, p[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def profile_traffic():
+    """DRAM bytes per attention launch from the committed ncu summary, if it matches the current kernel."""
+    try:
+        d = json.load(open(PROFILE_SUMMARY))
+        src = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()
+        if d.get("decode_cu_sha256") != src:
+            return None, "kernel changed since the ncu capture"
+        return float(d["dram_bytes_per_launch_full"]), d.get("note", "")
+    except Exception:
+        return None, "no ncu summary"
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+
+    import paged_kv_cache_302_gb300 as pa
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pa.load()
+    w = workload(args.steps, args.warmup)
+    nsteps = args.steps + args.warmup
+    pt = args.partition_tokens
+
+    # ---- build the cache state: allocate every context, write all K/V through slot_mapping
+    alloc = pa.BlockAllocator(w.NB, w.B, w.free_order)
+    prompt_len = w.ctx - 1                      # the decode step adds the last token
+    slots = []
+    for s in range(w.N):
+        alloc.add_seq(s)
+        if prompt_len[s] > 0:
+            slots.append(alloc.append_slots(s, int(prompt_len[s]))[0])
+    slots = np.concatenate(slots)
+    k, v = W.token_kv(w, slots.size)
+    dt = torch.bfloat16
+    pool = torch.zeros((w.NB, w.B, 2, w.H_kv, w.D), dtype=dt, device=dev)
+
+    def dev_bits(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(dt)
+
+    for lo in range(0, slots.size, 1 << 20):
+        hi = min(slots.size, lo + (1 << 20))
+        pa.pa_reshape_and_cache(dev_bits(k[lo:hi]), dev_bits(v[lo:hi]), pool, torch.from_numpy(slots[lo:hi]).to(dev))
+    del k, v
+    MB = w.max_blocks_per_seq(grow=2 * nsteps + 16)
+    seq_ids = list(range(w.N))
+    ones = np.ones(w.N, dtype=np.int32)
+
+    # ---- device-resident phase: allocation for every step done up front
+    step_inputs = W.decode_steps(w, nsteps)
+    slot_steps, ctx_steps = [], []
+    for i in range(nsteps):
+        sl, pairs = alloc.append_batch(seq_ids, ones)
+        assert pairs.size == 0
+        slot_steps.append(torch.from_numpy(sl).to(dev))
+        ctx_steps.append(torch.from_numpy(np.array([alloc.seq_len(s) for s in seq_ids], dtype=np.int32)).to(dev))
+    tables, _ = alloc.block_tables(seq_ids, MB)
+    tab = torch.from_numpy(tables).to(dev)
+    q_d = [dev_bits(x[0]) for x in step_inputs]
+    k_d = [dev_bits(x[1]) for x in step_inputs]
+    v_d = [dev_bits(x[2]) for x in step_inputs]
+    max_ctx = int(w.ctx.max()) + 2 * nsteps + 16
+    ws = torch.empty(pa.pa_decode_workspace_bytes(w.N, w.H_q, w.H_kv, w.D, max_ctx, pt), dtype=torch.uint8,
+                     device=dev)
+    out = torch.empty((w.N, w.H_q, w.D), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    per_tok = 2 * w.H_kv * w.D * w.elem_bytes
+    step_bytes = [int(c.sum().item()) * per_tok for c in ctx_steps]
+    stream = torch.cuda.current_stream()
+    att_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(nsteps)]
+
+    def step(i):
+        pa.pa_reshape_and_cache(k_d[i], v_d[i], pool, slot_steps[i], dev_err=err)
+        pa.pa_decode(out, q_d[i], pool, tab, ctx_steps[i], max_ctx, partition_tokens=pt, workspace=ws,
+                     dev_err=err, attend_events=att_ev[i])
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = pa.launch_count()
+    with ClockSampler(local) as clk:
+        time.sleep(0.2)
+        e0.record(stream)
+        for i in range(args.warmup, nsteps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    launches = pa.launch_count() - launches0
+    t_dev = e0.elapsed_time(e1) * 1e-3
+    attend_s = [att_ev[i][0].elapsed_time(att_ev[i][1]) * 1e-3 for i in range(args.warmup, nsteps)]
+    assert int(err.item()) == 0, f"device error flags {int(err.item())}"
+    timed_bytes = sum(step_bytes[args.warmup:])
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([t_dev], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_dev = float(tt.item())
+        bb = torch.tensor([float(timed_bytes)], device=dev)
+        dist.all_reduce(bb)
+        total_bytes = float(bb.item())
+    else:
+        total_bytes = float(timed_bytes)
+    value = total_bytes / t_dev / 1e9
+    ms_per_step = t_dev / args.steps * 1e3
+
+    # ---- roofline of the attention kernel
+    hbm, peak_src = peaks()
+    att_mean = sum(attend_s) / len(attend_s)
+    att_bytes = sum(step_bytes[args.warmup:]) / args.steps
+    achieved = att_bytes / att_mean / 1e9
+    traffic, traffic_note = profile_traffic()
+
+    # ---- end-to-end through the public API with host buffers
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    e2e_inputs = W.decode_steps(w, nsteps)
+    h_q = [pin(x[0].view(np.int16)) for x in e2e_inputs]
+    h_k = [pin(x[1].view(np.int16)) for x in e2e_inputs]
+    h_v = [pin(x[2].view(np.int16)) for x in e2e_inputs]
+    h_out = torch.empty((w.N, w.H_q, w.D), dtype=torch.float32).pin_memory()
+    h_tab = torch.empty((w.N, MB), dtype=torch.int32).pin_memory()
+    h_ctx = torch.empty(w.N, dtype=torch.int32).pin_memory()
+    h_slot = torch.empty(w.N, dtype=torch.int64).pin_memory()
+    d_q = torch.empty((w.N, w.H_q, w.D), dtype=dt, device=dev)
+    d_k = torch.empty((w.N, w.H_kv, w.D), dtype=dt, device=dev)
+    d_v = torch.empty_like(d_k)
+    d_tab = torch.empty((w.N, MB), dtype=torch.int32, device=dev)
+    d_ctx = torch.empty(w.N, dtype=torch.int32, device=dev)
+    d_slot = torch.empty(w.N, dtype=torch.int64, device=dev)
+    h2d = (h_q[0].numel() * 2 + h_k[0].numel() * 2 * 2 + h_tab.numel() * 4 + h_ctx.numel() * 4 + h_slot.numel() * 8)
+    d2h = h_out.numel() * 4
+    e2e_bytes = []
+
+    def e2e_step(i):
+        sl, pairs = alloc.append_batch(seq_ids, ones)
+        tbl, cx = alloc.block_tables(seq_ids, MB)
+        h_slot.numpy()[:] = sl
+        h_tab.numpy()[:] = tbl
+        h_ctx.numpy()[:] = cx
+        d_q.view(torch.int16).copy_(h_q[i], non_blocking=True)
+        d_k.view(torch.int16).copy_(h_k[i], non_blocking=True)
+        d_v.view(torch.int16).copy_(h_v[i], non_blocking=True)
+        d_tab.copy_(h_tab, non_blocking=True)
+        d_ctx.copy_(h_ctx, non_blocking=True)
+        d_slot.copy_(h_slot, non_blocking=True)
+        if pairs.size:
+            pa.pa_copy_blocks(pool, torch.from_numpy(pairs).to(dev), dev_err=err)
+        pa.pa_reshape_and_cache(d_k, d_v, pool, d_slot, dev_err=err)
+        pa.pa_decode(out, d_q, pool, d_tab, d_ctx, max_ctx, partition_tokens=pt, workspace=ws, dev_err=err)
+        h_out.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return int(cx.astype(np.int64).sum()) * per_tok
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for i in range(args.warmup, nsteps):
+        e2e_bytes.append(e2e_step(i))
+    t_e2e = time.perf_counter() - t0
+    e2e_value = sum(e2e_bytes) / t_e2e / 1e9
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([t_e2e, float(sum(e2e_bytes))], device=dev)
+        mx = tt[:1].clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        sm = tt[1:].clone()
+        dist.all_reduce(sm)
+        e2e_value = float(sm.item()) / float(mx.item()) / 1e9
+
+    # ---- CPU baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host_pool, tables_h, ctx_h, _ = host_state(w)
+        rate, cores, seqs, secs = oracle_sample_rate(w, host_pool, tables_h, ctx_h, W.queries(w), args.cpu_seconds)
+        cpu = {"value": rate, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"fp64 oracle, all {w.H_q} query heads of {seqs} of the {w.N} sequences "
+                         f"(first decode step's contexts), {secs:.1f} s wall"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(config_dict(w, pt), parallelism="independent replicas" if world > 1 else "1 GPU"),
+            "seq_steps_per_s": w.N * world / (t_dev / args.steps),
+            "pct_of_hbm_peak": 100.0 * value / world / hbm,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": traffic, "kernel": "attend_kernel<bf16,128,paged>",
+                         "bytes_per_launch": att_bytes, "per_unit": f"{per_tok} B per context token",
+                         "peak_source": peak_src, "traffic_note": traffic_note},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

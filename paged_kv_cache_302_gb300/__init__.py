@@ -154,11 +154,19 @@ def _stream_ptr(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _events_arg(events):
+def _events_arg(events, stream):
+    """Handles of two torch.cuda.Event objects for the library to record.
+
+    torch creates an event's handle lazily and only lets elapsed_time() read
+    events it has recorded itself, so both are recorded once here (creating
+    them); the library then records them again around the attention kernel,
+    which replaces these timestamps."""
     if events is None:
         return None
-    arr = (ctypes.c_void_p * 2)(events[0].cuda_event, events[1].cuda_event)
-    return arr
+    s = torch.cuda.current_stream() if stream is None else stream
+    for e in events[:2]:
+        e.record(s)
+    return (ctypes.c_void_p * 2)(events[0].cuda_event, events[1].cuda_event)
 
 
 # ----------------------------------------------------------------------------- device entry points
@@ -219,7 +227,7 @@ def pa_decode(out, q, pool, block_tables, ctx_lens, max_ctx, scale=None, partiti
                        _dev(block_tables, "block_tables", torch.int32), _dev(ctx_lens, "ctx_lens", torch.int32), N,
                        H_q, H_kv, D, B, MB, NB, int(max_ctx), scale, int(partition_tokens), _dev(ws, "workspace"),
                        ws.numel() * ws.element_size(), _dtype_code(pool.dtype), _err_ptr(dev_err),
-                       _events_arg(attend_events), _stream_ptr(stream)))
+                       _events_arg(attend_events, stream), _stream_ptr(stream)))
     return out
 
 
@@ -241,7 +249,7 @@ def pa_decode_contiguous(out, q, k_buf, v_buf, req_ids, ctx_lens, max_ctx, scale
                                   _dev(ctx_lens, "ctx_lens", torch.int32), N, H_q, H_kv, D, N_max, S_max,
                                   int(max_ctx), scale, int(partition_tokens), _dev(ws, "workspace"),
                                   ws.numel() * ws.element_size(), _dtype_code(k_buf.dtype), _err_ptr(dev_err),
-                                  _events_arg(attend_events), _stream_ptr(stream)))
+                                  _events_arg(attend_events, stream), _stream_ptr(stream)))
     return out
 
 
