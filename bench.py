@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--seqs", type=int, default=256,
+                    help="sequences (256 is the benchmarked workload; fewer for small profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
 
 
@@ -64,9 +67,9 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
 
 
-def workload(steps: int, warmup: int) -> W.Workload:
+def workload(steps: int, warmup: int, seqs: int = 256) -> W.Workload:
     # room for every decode step of the device and end-to-end phases
-    return W.llama3_8b(grow=2 * (steps + warmup) + 16)
+    return W.llama3_8b(n_seqs=seqs, grow=2 * (steps + warmup) + 16)
 
 
 def config_dict(w: W.Workload, pt: int) -> dict:
@@ -108,7 +111,7 @@ def run_reference(args):
         return 0
     import oracle
 
-    w = workload(args.steps, args.warmup)
+    w = workload(args.steps, args.warmup, args.seqs)
     host_pool, tables, ctx, slots = host_state(w)
     q = W.queries(w)
     nthreads = oracle.num_threads()
@@ -248,7 +251,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pa.load()
-    w = workload(args.steps, args.warmup)
+    w = workload(args.steps, args.warmup, args.seqs)
     nsteps = args.steps + args.warmup
     pt = args.partition_tokens
 
@@ -345,6 +348,54 @@ def run_ours(args):
     traffic, traffic_note = profile_traffic()
 
     # ---- end-to-end through the public API with host buffers
+    e2e_value, h2d, d2h = None, 0, 0
+    if not args.no_e2e:
+        e2e_value, h2d, d2h = run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world)
+
+    # ---- CPU baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host_pool, tables_h, ctx_h, _ = host_state(w)
+        rate, cores, seqs, secs = oracle_sample_rate(w, host_pool, tables_h, ctx_h, W.queries(w), args.cpu_seconds)
+        cpu = {"value": rate, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"fp64 oracle, all {w.H_q} query heads of {seqs} of the {w.N} sequences "
+                         f"(first decode step's contexts), {secs:.1f} s wall"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(config_dict(w, pt), parallelism="independent replicas" if world > 1 else "1 GPU"),
+            "seq_steps_per_s": w.N * world / (t_dev / args.steps),
+            "pct_of_hbm_peak": 100.0 * value / world / hbm,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": traffic, "kernel": "attend_kernel<bf16,128,paged>",
+                         "bytes_per_launch": att_bytes, "per_unit": f"{per_tok} B per context token",
+                         "peak_source": peak_src, "traffic_note": traffic_note},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world):
+    """Decode steps through the public API from pinned host buffers: host allocation, host->device copies of
+    the step's inputs, cache write, decode, device->host copy of the output, all inside the timed region."""
+    import torch
+
+    import paged_kv_cache_302_gb300 as pa
+
+    dt = torch.bfloat16
+    nsteps = args.steps + args.warmup
+    per_tok = 2 * w.H_kv * w.D * w.elem_bytes
+    seq_ids = list(range(w.N))
+    ones = np.ones(w.N, dtype=np.int32)
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
     e2e_inputs = W.decode_steps(w, nsteps)
     h_q = [pin(x[0].view(np.int16)) for x in e2e_inputs]
@@ -401,37 +452,7 @@ def run_ours(args):
         sm = tt[1:].clone()
         dist.all_reduce(sm)
         e2e_value = float(sm.item()) / float(mx.item()) / 1e9
-
-    # ---- CPU baseline (rank 0, N = 1 only)
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        host_pool, tables_h, ctx_h, _ = host_state(w)
-        rate, cores, seqs, secs = oracle_sample_rate(w, host_pool, tables_h, ctx_h, W.queries(w), args.cpu_seconds)
-        cpu = {"value": rate, "unit": "GB/s", "cores": cores, "kind": "oracle",
-               "sample": f"fp64 oracle, all {w.H_q} query heads of {seqs} of the {w.N} sequences "
-                         f"(first decode step's contexts), {secs:.1f} s wall"}
-
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": dict(config_dict(w, pt), parallelism="independent replicas" if world > 1 else "1 GPU"),
-            "seq_steps_per_s": w.N * world / (t_dev / args.steps),
-            "pct_of_hbm_peak": 100.0 * value / world / hbm,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": traffic, "kernel": "attend_kernel<bf16,128,paged>",
-                         "bytes_per_launch": att_bytes, "per_unit": f"{per_tok} B per context token",
-                         "peak_source": peak_src, "traffic_note": traffic_note},
-            "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches,
-            "clocks": clk.summary(),
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
-    return 0
+    return e2e_value, h2d, d2h
 
 
 def main():

@@ -12,7 +12,7 @@
 //     and writes one work record (seq, kv head, partition, ctx) per
 //     (partition, kv head) in longest-first order: whole partitions in sequence
 //     order, then the ragged last partitions by decreasing length.
-//  2. attend_kernel (persistent, ~3 CTAs per SM, 2 warps each): CTA c takes
+//  2. attend_kernel (persistent, 4 CTAs per SM, 2 warps each): CTA c takes
 //     records c, c + grid, ...  Warp 1 (producer) streams each record's K/V
 //     through a ring of shared-memory stages with TMA: one 5-D tensor copy per
 //     KV block brings the block's K and V rows of one head, 128-byte swizzled;
@@ -721,7 +721,7 @@ static pa_status run_attend(const DecodeArgs& a, const WorkspaceLayout& L, const
     int sms = 0, smem_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-    const int ctas_wanted = std::max(1, env_int("PA_DECODE_CTAS_PER_SM", 3));
+    const int ctas_wanted = std::max(1, env_int("PA_DECODE_CTAS_PER_SM", 4));
     int nstage = env_int("PA_DECODE_STAGES", 0);
     if (nstage <= 0) {
         const long budget = (long)smem_sm / ctas_wanted - 1024;
