@@ -146,6 +146,31 @@ pa_status pa_decode_contiguous(void* out, pa_dtype out_dtype, const void* q, con
                                void* stream);
 
 /* ------------------------------------------------------------------------
+ * pa_decode without a caller-provided workspace.  The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate device
+ * memory where they decode (a plug-in inside a framework that owns every
+ * allocation, a serving loop that must not allocate after start-up, an engine
+ * that has already carved up all of HBM).  Arguments and results are those of
+ * pa_decode minus `workspace` / `ws_bytes`.
+ * - Scratch space: a file-scope device array of PA_STATIC_WORKSPACE_BYTES
+ *   (32 MiB) inside libpa.so.  Every GPU that loads the library holds it until
+ *   the process exits.  A batch whose pa_decode_workspace_bytes(...) exceeds
+ *   it is rejected with PA_ERR_UNSUPPORTED and a message; nothing is launched.
+ * - The first call on a device looks up the array's device address for that
+ *   device (cudaGetSymbolAddress with the device current); make that first
+ *   call before any stream capture.  The call allocates nothing.
+ * - All calls share the one array and it keeps the last call's contents; the
+ *   kernels rewrite every part of it they read, so nothing needs clearing.
+ *   Calls that overlap on the GPU (different streams, or threads) race on it:
+ *   order them on one stream or use pa_decode with separate workspaces.
+ * ---------------------------------------------------------------------- */
+#define PA_STATIC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const void* q, const void* pool,
+                             const int32_t* block_tables, const int32_t* ctx_lens, int N, int H_q, int H_kv, int D,
+                             int B, int MB, int NB, int max_ctx, float scale, int partition_tokens,
+                             pa_dtype kv_dtype, int* dev_err, void* const* attend_events, void* stream);
+
+/* ------------------------------------------------------------------------
  * Merge of split-context partials (the running maximum / exponential sum /
  * unnormalised output the block-by-block online softmax keeps, [PA]
  * アルゴリズムの擬似コード, taken per partition and combined).

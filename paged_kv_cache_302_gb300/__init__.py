@@ -74,6 +74,8 @@ def _declare(L):
         "pa_decode_contiguous": ([P, i32, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, f32, i32, P, sz, i32, P, P,
                                   P], i32),
         "pa_partition_reduce": ([P, i32, P, P, P, P, i32, i32, i32, P, P], i32),
+        "pa_decode_no_alloc": ([P, i32, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, i32, P, P, P],
+                               i32),
         "pa_alloc_create": ([i32, i32, P, ctypes.POINTER(ctypes.c_void_p)], i32),
         "pa_alloc_destroy": ([P], None),
         "pa_alloc_add_seq": ([P, i32], i32),
@@ -228,6 +230,34 @@ def pa_decode(out, q, pool, block_tables, ctx_lens, max_ctx, scale=None, partiti
                        H_q, H_kv, D, B, MB, NB, int(max_ctx), scale, int(partition_tokens), _dev(ws, "workspace"),
                        ws.numel() * ws.element_size(), _dtype_code(pool.dtype), _err_ptr(dev_err),
                        _events_arg(attend_events, stream), _stream_ptr(stream)))
+    return out
+
+
+PA_STATIC_WORKSPACE_BYTES = 32 * 1024 * 1024
+
+
+def pa_decode_no_alloc(out, q, pool, block_tables, ctx_lens, max_ctx, scale=None, partition_tokens=0, dev_err=None,
+                       attend_events=None, stream=None):
+    """pa_decode with the library's built-in workspace: allocates no device memory.
+
+    For callers that cannot allocate device memory where they decode.  The
+    batch's workspace must fit in PA_STATIC_WORKSPACE_BYTES; calls that overlap
+    on the GPU share (and race on) the one built-in workspace.  The first call
+    on a device should come before any stream capture."""
+    N, H_q, D = q.shape
+    NB, B, _, H_kv, D2 = pool.shape
+    MB = block_tables.shape[1]
+    if D2 != D or tuple(out.shape) != (N, H_q, D) or q.dtype != pool.dtype:
+        raise PAError(PA_ERR_INVALID, "shape/dtype mismatch")
+    if tuple(block_tables.shape) != (N, MB) or ctx_lens.numel() != N:
+        raise PAError(PA_ERR_INVALID, "block_tables must be [N, MB] and ctx_lens [N]")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    L = load()
+    _check(L.pa_decode_no_alloc(_dev(out, "out"), _dtype_code(out.dtype), _dev(q, "q"), _dev(pool, "pool"),
+                                _dev(block_tables, "block_tables", torch.int32),
+                                _dev(ctx_lens, "ctx_lens", torch.int32), N, H_q, H_kv, D, B, MB, NB, int(max_ctx),
+                                scale, int(partition_tokens), _dtype_code(pool.dtype), _err_ptr(dev_err),
+                                _events_arg(attend_events, stream), _stream_ptr(stream)))
     return out
 
 
