@@ -42,8 +42,8 @@ DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_302_gb300", "csrc", "decode.cu")
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -185,7 +185,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except Exception:
@@ -194,7 +194,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which: str):
+        setattr(self, which, time.time())
 
     def __exit__(self, *a):
         if self.proc:
@@ -205,9 +208,13 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        """Samples taken between mark('t0') and mark('t1') (the timed region)."""
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        t0, t1 = getattr(self, "t0", 0.0), getattr(self, "t1", float("inf"))
+        for t, ln in self.lines:
+            if not (t0 <= t <= t1 + 0.025):
+                continue
             p = [x.strip() for x in ln.split(",")]
             if len(p) < 9:
                 continue
@@ -302,10 +309,10 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     att_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(nsteps)]
 
-    def step(i):
+    def step(i, events=None):
         pa.pa_reshape_and_cache(k_d[i], v_d[i], pool, slot_steps[i], dev_err=err)
         pa.pa_decode(out, q_d[i], pool, tab, ctx_steps[i], max_ctx, partition_tokens=pt, workspace=ws,
-                     dev_err=err, attend_events=att_ev[i])
+                     dev_err=err, attend_events=events)
 
     for i in range(args.warmup):
         step(i)
@@ -316,14 +323,21 @@ def run_ours(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = pa.launch_count()
     with ClockSampler(local) as clk:
-        time.sleep(0.2)
+        time.sleep(0.5)                      # let the sampler start
+        clk.mark("t0")
         e0.record(stream)
         for i in range(args.warmup, nsteps):
             step(i)
         e1.record(stream)
         torch.cuda.synchronize()
+        clk.mark("t1")
     launches = pa.launch_count() - launches0
     t_dev = e0.elapsed_time(e1) * 1e-3
+    # the attention kernel alone: the same steps again with events around it (an event between the
+    # schedule and attention kernels stops their overlap, so these runs are not part of `value`)
+    for i in range(args.warmup, nsteps):
+        step(i, att_ev[i])
+    torch.cuda.synchronize()
     attend_s = [att_ev[i][0].elapsed_time(att_ev[i][1]) * 1e-3 for i in range(args.warmup, nsteps)]
     assert int(err.item()) == 0, f"device error flags {int(err.item())}"
     timed_bytes = sum(step_bytes[args.warmup:])
@@ -392,7 +406,8 @@ def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world):
     import paged_kv_cache_302_gb300 as pa
 
     dt = torch.bfloat16
-    nsteps = args.steps + args.warmup
+    e2e_steps = min(args.steps, 30)
+    nsteps = e2e_steps + args.warmup
     per_tok = 2 * w.H_kv * w.D * w.elem_bytes
     seq_ids = list(range(w.N))
     ones = np.ones(w.N, dtype=np.int32)

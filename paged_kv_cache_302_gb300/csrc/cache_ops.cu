@@ -15,6 +15,8 @@ __global__ void __launch_bounds__(128) reshape_and_cache_kernel(const uint4* __r
                                                                 const uint4* __restrict__ v, uint4* __restrict__ pool,
                                                                 const int64_t* __restrict__ slots, int T,
                                                                 int64_t nslots, int row_vec, int B, int* err) {
+    griddep_wait();
+    griddep_launch_dependents();
     for (int i = blockIdx.x; i < T; i += gridDim.x) {
         const int64_t slot = slots[i];
         if (slot < 0) continue;
@@ -41,11 +43,10 @@ pa_status launch_reshape_and_cache(const void* k, const void* v, void* pool, con
     if (T == 0) return PA_OK;
     const int row_vec = H_kv * D * 2 / 16;
     int grid = T < 152 * 16 ? T : 152 * 16;
-    reshape_and_cache_kernel<<<grid, 128, 0, stream>>>(static_cast<const uint4*>(k), static_cast<const uint4*>(v),
-                                                       static_cast<uint4*>(pool), slot_mapping, T,
-                                                       (int64_t)NB * B, row_vec, B, dev_err);
+    cudaError_t e = launch_kernel(reshape_and_cache_kernel, dim3(grid), dim3(128), 0, stream,
+                                  static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+                                  static_cast<uint4*>(pool), slot_mapping, T, (int64_t)NB * B, row_vec, B, dev_err);
     count_launch();
-    cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "reshape_and_cache launch");
 }
 
@@ -57,6 +58,8 @@ constexpr int kCopyUnroll = 4;
 __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(uint4* __restrict__ pool,
                                                                    const int64_t* __restrict__ pairs, int n, int NB,
                                                                    int64_t blk_vec, int* err) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int i = blockIdx.x;
     const int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
     if (src < 0 || src >= NB || dst < 0 || dst >= NB) {
@@ -97,9 +100,9 @@ pa_status launch_copy_blocks(void* pool, const int64_t* pairs, int n, int NB, in
     int64_t gy = (blk_vec + chunk - 1) / chunk;
     if (gy > 65535) gy = 65535;
     dim3 grid(n, (unsigned)gy);
-    copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(static_cast<uint4*>(pool), pairs, n, NB, blk_vec, dev_err);
+    cudaError_t e = launch_kernel(copy_blocks_kernel, grid, dim3(kCopyThreads), 0, stream, static_cast<uint4*>(pool),
+                                  pairs, n, NB, blk_vec, dev_err);
     count_launch();
-    cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "copy_blocks launch");
 }
 

@@ -2,6 +2,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "pa_internal.h"
@@ -24,6 +25,14 @@ pa_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("PA_NO_PDL");
+        return !(v && *v && *v != '0');
+    }();
+    return on;
+}
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

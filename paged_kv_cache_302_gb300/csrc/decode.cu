@@ -22,6 +22,9 @@
 //     an online softmax in base 2 between stages, and writes the normalised
 //     output, or the partition's (m2, l, acc) when the context has several.
 //  3. partition_reduce_kernel: merges the partials of multi-partition rows.
+// Each kernel is launched with programmatic stream serialisation, so its CTAs
+// start while the previous kernel drains and wait (griddepcontrol.wait)
+// before touching memory.
 #include <cuda.h>
 
 #include <algorithm>
@@ -95,45 +98,57 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
     return v;
 }
 
-__device__ __forceinline__ int size_bin(int tokens) {
+// Records for ragged last partitions are ordered by decreasing length through
+// bins of kStageTok tokens (the top bin collects everything longer).
+__device__ __forceinline__ int size_bin(int tokens, int nbins) {
     const int b = (tokens + kStageTok - 1) / kStageTok;
-    return b < kNumBins ? b : kNumBins - 1;
+    return b < nbins ? b : nbins - 1;
+}
+
+static int plan_bins(int PT, int max_ctx) {
+    const int longest_tail = PT >= kUnpartitioned ? max_ctx : PT - 1;
+    const int n = (longest_tail + kStageTok - 1) / kStageTok + 1;
+    return n < kNumBins ? n : kNumBins;
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ ctx_lens,
                                                             const int32_t* __restrict__ req_ids, int N, int H_kv,
-                                                            int PT, int max_ctx, int cap, int N_max,
-                                                            int* __restrict__ header, int* __restrict__ nparts,
-                                                            int4* __restrict__ rec, int* err) {
+                                                            int PT, int max_ctx, int cap, int N_max, int nbins,
+                                                            int* __restrict__ header, int4* __restrict__ rec,
+                                                            int* __restrict__ nparts, int* err) {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ int bins[kNumBins];
     __shared__ int warp_sum[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    for (int b = tid; b < kNumBins; b += blockDim.x) bins[b] = 0;
+    for (int b = tid; b < nbins; b += blockDim.x) bins[b] = 0;
     const int per = (N + blockDim.x - 1) / blockDim.x;
     const int s_begin = min(N, tid * per), s_end = min(N, s_begin + per);
+    // context length of sequence s, 0 for an invalid length, -1 for an invalid request id
+    auto checked_ctx = [&](int s) -> int {
+        const int c = ctx_lens[s];
+        if (c < 1 || c > max_ctx || c > cap) return 0;
+        if (req_ids) {
+            const int r = req_ids[s];
+            if (r < 0 || r >= N_max) return -1;
+        }
+        return c;
+    };
     __syncthreads();
 
-    // pass 1: partitions per sequence, whole-partition count, histogram of ragged tails
+    // pass 1: whole partitions per thread, histogram of ragged tails
     int my_full = 0;
     for (int s = s_begin; s < s_end; ++s) {
-        const int c = ctx_lens[s];
-        bool bad = c < 1 || c > max_ctx || c > cap;
-        if (bad) flag_error(err, PA_DEV_ERR_CTX);
-        if (!bad && req_ids) {
-            const int r = req_ids[s];
-            if (r < 0 || r >= N_max) {
-                bad = true;
-                flag_error(err, PA_DEV_ERR_REQ);
-            }
-        }
-        if (bad) {
+        const int c = checked_ctx(s);
+        if (c <= 0) {
+            flag_error(err, c == 0 ? PA_DEV_ERR_CTX : PA_DEV_ERR_REQ);
             nparts[s] = 0;
             continue;
         }
         const int nf = c / PT, rem = c - nf * PT;
         nparts[s] = nf + (rem > 0);
         my_full += nf;
-        if (rem > 0) atomicAdd(&bins[size_bin(rem)], 1);
+        if (rem > 0) atomicAdd(&bins[size_bin(rem, nbins)], 1);
     }
 
     // exclusive scan of whole partitions in sequence order
@@ -150,34 +165,47 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     int full_pos = incl - my_full + (warp ? warp_sum[warp - 1] : 0);
     __syncthreads();
 
-    // descending exclusive scan of the tail histogram: largest tails first
+    // descending exclusive scan of the tail histogram: longest tails first
     if (warp == 0) {
-        constexpr int kPerLane = kNumBins / 32;
-        const int top = kNumBins - 1 - lane * kPerLane;
+        const int chunk = (nbins + 31) / 32;
         int sum = 0;
-        for (int i = 0; i < kPerLane; ++i) sum += bins[top - i];
+        for (int j = lane * chunk; j < min(nbins, (lane + 1) * chunk); ++j) sum += bins[nbins - 1 - j];
         const int tincl = warp_incl_scan(sum);
         int run = full_total + tincl - sum;
-        for (int i = 0; i < kPerLane; ++i) {
-            const int c = bins[top - i];
-            bins[top - i] = run;
+        for (int j = lane * chunk; j < min(nbins, (lane + 1) * chunk); ++j) {
+            const int c = bins[nbins - 1 - j];
+            bins[nbins - 1 - j] = run;
             run += c;
         }
         if (lane == 31) header[0] = (full_total + tincl) * H_kv;
     }
     __syncthreads();
 
-    // pass 2: write the records, one per (partition, kv head)
+    // pass 2: one record per (partition, kv head)
     for (int s = s_begin; s < s_end; ++s) {
-        if (nparts[s] == 0) continue;
-        const int c = ctx_lens[s];
+        const int c = checked_ctx(s);
+        if (c <= 0) continue;
         const int nf = c / PT, rem = c - nf * PT;
         for (int p = 0; p < nf; ++p, ++full_pos)
             for (int h = 0; h < H_kv; ++h) rec[(size_t)full_pos * H_kv + h] = make_int4(s, h, p, c);
         if (rem > 0) {
-            const int pos = atomicAdd(&bins[size_bin(rem)], 1);
+            const int pos = atomicAdd(&bins[size_bin(rem, nbins)], 1);
             for (int h = 0; h < H_kv; ++h) rec[(size_t)pos * H_kv + h] = make_int4(s, h, nf, c);
         }
+    }
+}
+
+// ============================================================================= merge of partition partials
+
+template <typename OutT, int D>
+__device__ __forceinline__ void store_row(OutT* dst, const float (&o)[D / 32]) {
+    constexpr int V = D / 32;
+    const int lane = threadIdx.x & 31;
+    if constexpr (sizeof(OutT) == 4 && V == 4) {
+        *reinterpret_cast<float4*>(dst + lane * V) = make_float4(o[0], o[1], o[2], o[3]);
+    } else {
+#pragma unroll
+        for (int v = 0; v < V; ++v) dst[lane * V + v] = from_float<OutT>(o[v]);
     }
 }
 
@@ -248,6 +276,9 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
         if (!PAGED) prefetch_tmap(&tm_b);
     }
     __syncthreads();
+    // everything above overlaps the schedule kernel; from here on its records are needed
+    griddep_wait();
+    griddep_launch_dependents();
 
     const int lane = threadIdx.x & 31;
     const int Beff = PAGED ? p.B : kStageTok;  // tokens per TMA box along the token axis
@@ -593,83 +624,103 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
 
 // ============================================================================= 3. partition merge
 
+// One CTA per output row.  The partitions are dealt round-robin to the CTA's
+// warps; every lane owns D/32 consecutive elements.  All warps first find the
+// row's largest m2 (one load per partition and lane), then each accumulates
+// 2^(m2_p - M) * acc_p and 2^(m2_p - M) * l_p over its partitions with the
+// loads of four partitions in flight, and warp 0 adds the warps' sums.
+constexpr int kReduceWarps = 8;
+
 template <typename OutT, int D>
-__global__ void __launch_bounds__(256) partition_reduce_kernel(OutT* __restrict__ out, const float* __restrict__ m2,
-                                                               const float* __restrict__ l,
-                                                               const float* __restrict__ acc,
-                                                               const int32_t* __restrict__ nparts, int rows_per_seq,
-                                                               int R, int P, int skip_single, int* err) {
-    constexpr int V = D / 32;  // elements per lane
-    const int lane = threadIdx.x & 31;
-    const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+__global__ void __launch_bounds__(kReduceWarps * 32) partition_reduce_kernel(
+    OutT* __restrict__ out, const float* __restrict__ m2, const float* __restrict__ l, const float* __restrict__ acc,
+    const int32_t* __restrict__ nparts, int rows_per_seq, int R, int P, int skip_single, int* err) {
+    constexpr int V = D / 32;
+    __shared__ float part_o[kReduceWarps][D];
+    __shared__ float part_den[kReduceWarps];
+    griddep_wait();
+    griddep_launch_dependents();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int r = blockIdx.x;
     if (r >= R) return;
     const int np = nparts[r / rows_per_seq];
-    if (skip_single) {
-        if (np <= 1) return;  // written by the attention kernel (or an invalid sequence)
-    }
+    if (skip_single && np <= 1) return;  // written by the attention kernel, or an invalid sequence
     if (np < 1 || np > P) {
-        if (lane == 0) flag_error(err, PA_DEV_ERR_CTX);
+        if (threadIdx.x == 0) flag_error(err, PA_DEV_ERR_CTX);
         return;
     }
     const float* mr = m2 + (size_t)r * P;
     const float* lr = l + (size_t)r * P;
-    const float* ar = acc + (size_t)r * P * D;
+    const float* ar = acc + (size_t)r * P * D + lane * V;
     float M = -INFINITY;
     for (int i = lane; i < np; i += 32) M = fmaxf(M, mr[i]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float den = 0.f;
-    for (int i = lane; i < np; i += 32) den += fast_exp2(mr[i] - M) * lr[i];
+    for (int k = 16; k > 0; k >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, k));
+    float o[V], den = 0.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    float o_[V];
-#pragma unroll
-    for (int v = 0; v < V; ++v) o_[v] = 0.f;
-    for (int i = 0; i < np; ++i) {
+    for (int v = 0; v < V; ++v) o[v] = 0.f;
+#pragma unroll 4
+    for (int i = warp; i < np; i += kReduceWarps) {
         const float w = fast_exp2(mr[i] - M);
-        const float* a = ar + (size_t)i * D + lane * V;
+        den += w * lr[i];
         if constexpr (V == 4) {
-            const float4 x = *reinterpret_cast<const float4*>(a);
-            o_[0] += w * x.x;
-            o_[1] += w * x.y;
-            o_[2] += w * x.z;
-            o_[3] += w * x.w;
+            const float4 x = *reinterpret_cast<const float4*>(ar + (size_t)i * D);
+            o[0] += w * x.x;
+            o[1] += w * x.y;
+            o[2] += w * x.z;
+            o[3] += w * x.w;
         } else {
-#pragma unroll
-            for (int v = 0; v < V; ++v) o_[v] += w * a[v];
+            const float2 x = *reinterpret_cast<const float2*>(ar + (size_t)i * D);
+            o[0] += w * x.x;
+            o[1] += w * x.y;
         }
     }
-    const float inv = 1.f / den;
-    OutT* dst = out + (size_t)r * D + lane * V;
 #pragma unroll
-    for (int v = 0; v < V; ++v) dst[v] = from_float<OutT>(o_[v] * inv);
+    for (int v = 0; v < V; ++v) part_o[warp][lane * V + v] = o[v];
+    if (lane == 0) part_den[warp] = den;
+    __syncthreads();
+    if (warp == 0) {
+        float d = 0.f;
+#pragma unroll
+        for (int w = 0; w < kReduceWarps; ++w) d += part_den[w];
+        const float inv = 1.f / d;
+        float res[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            float t = 0.f;
+#pragma unroll
+            for (int w = 0; w < kReduceWarps; ++w) t += part_o[w][lane * V + v];
+            res[v] = t * inv;
+        }
+        store_row<OutT, D>(out + (size_t)r * D, res);
+    }
 }
 
 template <typename OutT>
-static void reduce_dispatch_d(void* out, const float* m2, const float* l, const float* acc, const int32_t* nparts,
-                              int rows_per_seq, int R, int P, int D, bool skip, int* err, cudaStream_t st) {
-    const int grid = (R + 7) / 8;
+static cudaError_t reduce_dispatch_d(void* out, const float* m2, const float* l, const float* acc,
+                                     const int32_t* nparts, int rows_per_seq, int R, int P, int D, bool skip,
+                                     int* err, cudaStream_t st) {
+    const dim3 grid(R), block(kReduceWarps * 32);
     if (D == 128)
-        partition_reduce_kernel<OutT, 128><<<grid, 256, 0, st>>>(static_cast<OutT*>(out), m2, l, acc, nparts,
-                                                                 rows_per_seq, R, P, skip ? 1 : 0, err);
-    else
-        partition_reduce_kernel<OutT, 64><<<grid, 256, 0, st>>>(static_cast<OutT*>(out), m2, l, acc, nparts,
-                                                                rows_per_seq, R, P, skip ? 1 : 0, err);
+        return launch_kernel(partition_reduce_kernel<OutT, 128>, grid, block, 0, st, static_cast<OutT*>(out), m2, l,
+                             acc, nparts, rows_per_seq, R, P, skip ? 1 : 0, err);
+    return launch_kernel(partition_reduce_kernel<OutT, 64>, grid, block, 0, st, static_cast<OutT*>(out), m2, l, acc,
+                         nparts, rows_per_seq, R, P, skip ? 1 : 0, err);
 }
 
 pa_status launch_partition_reduce(void* out, int out_dtype, const float* m2, const float* l, const float* acc,
                                   const int32_t* nparts, int rows_per_seq, int R, int P, int D, bool skip_single,
                                   int* dev_err, cudaStream_t stream) {
     if (R == 0) return PA_OK;
+    cudaError_t e;
     if (out_dtype == PA_F32)
-        reduce_dispatch_d<float>(out, m2, l, acc, nparts, rows_per_seq, R, P, D, skip_single, dev_err, stream);
+        e = reduce_dispatch_d<float>(out, m2, l, acc, nparts, rows_per_seq, R, P, D, skip_single, dev_err, stream);
     else if (out_dtype == PA_F16)
-        reduce_dispatch_d<__half>(out, m2, l, acc, nparts, rows_per_seq, R, P, D, skip_single, dev_err, stream);
+        e = reduce_dispatch_d<__half>(out, m2, l, acc, nparts, rows_per_seq, R, P, D, skip_single, dev_err, stream);
     else
-        reduce_dispatch_d<__nv_bfloat16>(out, m2, l, acc, nparts, rows_per_seq, R, P, D, skip_single, dev_err,
-                                         stream);
+        e = reduce_dispatch_d<__nv_bfloat16>(out, m2, l, acc, nparts, rows_per_seq, R, P, D, skip_single, dev_err,
+                                             stream);
     count_launch();
-    cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "partition_reduce launch");
 }
 
@@ -765,9 +816,8 @@ static pa_status run_attend(const DecodeArgs& a, const WorkspaceLayout& L, const
         e = cudaEventRecord(static_cast<cudaEvent_t>(a.attend_events[0]), a.stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     }
-    kern<<<grid, kAttnThreads, smem, a.stream>>>(ta, tb, p);
+    e = launch_kernel(kern, dim3(grid), dim3(kAttnThreads), smem, a.stream, ta, tb, p);
     count_launch();
-    e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
     if (a.attend_events && a.attend_events[1]) {
         e = cudaEventRecord(static_cast<cudaEvent_t>(a.attend_events[1]), a.stream);
@@ -816,10 +866,10 @@ pa_status launch_decode(const DecodeArgs& a) {
     int* nparts = reinterpret_cast<int*>(ws + L.nparts);
     int4* rec = reinterpret_cast<int4*>(ws + L.records);
     const int cap = a.paged ? a.MB * a.B : a.S_max;
-    plan_kernel<<<1, kPlanThreads, 0, a.stream>>>(a.ctx_lens, a.paged ? nullptr : a.req_ids, a.N, a.H_kv, L.PT,
-                                                 a.max_ctx, cap, a.N_max, header, nparts, rec, a.dev_err);
+    cudaError_t e = launch_kernel(plan_kernel, dim3(1), dim3(kPlanThreads), 0, a.stream, a.ctx_lens,
+                                  a.paged ? nullptr : a.req_ids, a.N, a.H_kv, L.PT, a.max_ctx, cap, a.N_max,
+                                  plan_bins(L.PT, a.max_ctx), header, rec, nparts, a.dev_err);
     count_launch();
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "plan launch");
 
     const long maxrec_l = (long)a.N * L.P * a.H_kv;
@@ -831,13 +881,10 @@ pa_status launch_decode(const DecodeArgs& a) {
     else
         st = a.D == 128 ? dispatch_paged<__half, 128>(a, L, ta, tb, maxrec)
                         : dispatch_paged<__half, 64>(a, L, ta, tb, maxrec);
-    if (st != PA_OK) return st;
-    if (L.P > 1)
-        return launch_partition_reduce(a.out, a.out_dtype, reinterpret_cast<float*>(ws + L.part_m2),
-                                       reinterpret_cast<float*>(ws + L.part_l),
-                                       reinterpret_cast<float*>(ws + L.part_acc), nparts, a.H_q, a.N * a.H_q, L.P,
-                                       a.D, true, a.dev_err, a.stream);
-    return PA_OK;
+    if (st != PA_OK || L.P == 1) return st;
+    return launch_partition_reduce(a.out, a.out_dtype, reinterpret_cast<float*>(ws + L.part_m2),
+                                   reinterpret_cast<float*>(ws + L.part_l), reinterpret_cast<float*>(ws + L.part_acc),
+                                   nparts, a.H_q, a.N * a.H_q, L.P, a.D, true, a.dev_err, a.stream);
 }
 
 }  // namespace pa

@@ -6,6 +6,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pa_internal.h"
 
 namespace pa {
@@ -25,6 +27,39 @@ __device__ __forceinline__ uint64_t global_ns() {
 // A wait gives up after this many nanoseconds (the kernel then flags
 // PA_DEV_ERR_TIMEOUT and returns).  Legitimate waits last microseconds.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// ----------------------------------------------------------------------------- programmatic dependent launch
+
+// Blocks until the kernel launched before this one on the stream has finished
+// and its memory is visible (a no-op when the launch did not allow overlap).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel on the stream start its CTAs (they still wait in
+// griddep_wait before touching memory this kernel writes).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Host: launch with programmatic stream serialisation allowed, so the kernel's
+// CTAs may start while the previous kernel drains (every kernel of this
+// library calls griddep_wait before reading or writing global memory).
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                 Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ----------------------------------------------------------------------------- shared memory / mbarrier
 

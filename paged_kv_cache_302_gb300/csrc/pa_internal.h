@@ -31,7 +31,7 @@ constexpr int kUnpartitioned = 1 << 30;
 
 struct WorkspaceLayout {
     size_t header;     // int[4]: record count, spare
-    size_t nparts;     // int[N]
+    size_t nparts;     // int[N]: partitions per sequence (0 for an invalid one)
     size_t records;    // int4[N * P * H_kv]
     size_t part_m2;    // float[N * H_q * P]
     size_t part_l;     // float[N * H_q * P]
@@ -75,5 +75,6 @@ pa_status launch_decode(const DecodeArgs& a);
 pa_status launch_partition_reduce(void* out, int out_dtype, const float* m2, const float* l, const float* acc,
                                   const int32_t* nparts, int rows_per_seq, int R, int P, int D, bool skip_single,
                                   int* dev_err, cudaStream_t stream);
+bool pdl_enabled();
 
 }  // namespace pa
