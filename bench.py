@@ -232,14 +232,25 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def profile_traffic():
-    """DRAM bytes per attention launch from the committed ncu summary, if it matches the current kernel."""
+DEVICE_HDR = os.path.join(ROOT, "paged_kv_cache_302_gb300", "csrc", "pa_device.cuh")
+
+
+def attend_source_sha256() -> str:
+    """Hash of the attention kernel's source: its template in decode.cu plus the device helpers."""
+    src = open(DECODE_SRC).read()
+    a = src.index("// ============================================================================= 2. attention")
+    b = src.index("// ============================================================================= merge of partition")
+    return hashlib.sha256((src[a:b] + open(DEVICE_HDR).read()).encode()).hexdigest()
+
+
+def profile_traffic(bytes_per_launch: float):
+    """DRAM bytes per attention launch: the committed ncu capture's DRAM bytes per algorithmic byte, scaled to
+    this launch (traffic grows with the context tokens), if the kernel is unchanged since the capture."""
     try:
         d = json.load(open(PROFILE_SUMMARY))
-        src = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()
-        if d.get("decode_cu_sha256") != src:
-            return None, "kernel changed since the ncu capture"
-        return float(d["dram_bytes_per_launch_full"]), d.get("note", "")
+        if d.get("attend_source_sha256") != attend_source_sha256():
+            return None, "attention kernel changed since the ncu capture"
+        return float(d["dram_bytes_per_algorithmic_byte"]) * bytes_per_launch, d.get("note", "")
     except Exception:
         return None, "no ncu summary"
 
@@ -359,7 +370,7 @@ def run_ours(args):
     att_mean = sum(attend_s) / len(attend_s)
     att_bytes = sum(step_bytes[args.warmup:]) / args.steps
     achieved = att_bytes / att_mean / 1e9
-    traffic, traffic_note = profile_traffic()
+    traffic, traffic_note = profile_traffic(att_bytes)
 
     # ---- end-to-end through the public API with host buffers
     e2e_value, h2d, d2h = None, 0, 0

@@ -624,11 +624,10 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
 
 // ============================================================================= 3. partition merge
 
-// One CTA per output row.  The partitions are dealt round-robin to the CTA's
-// warps; every lane owns D/32 consecutive elements.  All warps first find the
-// row's largest m2 (one load per partition and lane), then each accumulates
-// 2^(m2_p - M) * acc_p and 2^(m2_p - M) * l_p over its partitions with the
-// loads of four partitions in flight, and warp 0 adds the warps' sums.
+// One warp per output row, 8 rows per CTA, so the whole merge is one wave of
+// short-lived warps.  Lane j holds the weight 2^(m2_p - M) of partitions
+// p = j, j+32, ...; the weighted sum over partitions broadcasts each weight
+// and keeps eight partitions' loads in flight.
 constexpr int kReduceWarps = 8;
 
 template <typename OutT, int D>
@@ -636,17 +635,15 @@ __global__ void __launch_bounds__(kReduceWarps * 32) partition_reduce_kernel(
     OutT* __restrict__ out, const float* __restrict__ m2, const float* __restrict__ l, const float* __restrict__ acc,
     const int32_t* __restrict__ nparts, int rows_per_seq, int R, int P, int skip_single, int* err) {
     constexpr int V = D / 32;
-    __shared__ float part_o[kReduceWarps][D];
-    __shared__ float part_den[kReduceWarps];
     griddep_wait();
     griddep_launch_dependents();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int r = blockIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * kReduceWarps + (threadIdx.x >> 5);
     if (r >= R) return;
     const int np = nparts[r / rows_per_seq];
     if (skip_single && np <= 1) return;  // written by the attention kernel, or an invalid sequence
     if (np < 1 || np > P) {
-        if (threadIdx.x == 0) flag_error(err, PA_DEV_ERR_CTX);
+        if (lane == 0) flag_error(err, PA_DEV_ERR_CTX);
         return;
     }
     const float* mr = m2 + (size_t)r * P;
@@ -659,48 +656,41 @@ __global__ void __launch_bounds__(kReduceWarps * 32) partition_reduce_kernel(
     float o[V], den = 0.f;
 #pragma unroll
     for (int v = 0; v < V; ++v) o[v] = 0.f;
-#pragma unroll 4
-    for (int i = warp; i < np; i += kReduceWarps) {
-        const float w = fast_exp2(mr[i] - M);
-        den += w * lr[i];
-        if constexpr (V == 4) {
-            const float4 x = *reinterpret_cast<const float4*>(ar + (size_t)i * D);
-            o[0] += w * x.x;
-            o[1] += w * x.y;
-            o[2] += w * x.z;
-            o[3] += w * x.w;
-        } else {
-            const float2 x = *reinterpret_cast<const float2*>(ar + (size_t)i * D);
-            o[0] += w * x.x;
-            o[1] += w * x.y;
+    for (int base = 0; base < np; base += 32) {
+        const int mine = base + lane;
+        const float w = mine < np ? fast_exp2(mr[mine] - M) : 0.f;
+        if (mine < np) den += w * lr[mine];
+        const int n = min(32, np - base);
+#pragma unroll 8
+        for (int j = 0; j < n; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, w, j);
+            const float* a = ar + (size_t)(base + j) * D;
+            if constexpr (V == 4) {
+                const float4 x = *reinterpret_cast<const float4*>(a);
+                o[0] += wj * x.x;
+                o[1] += wj * x.y;
+                o[2] += wj * x.z;
+                o[3] += wj * x.w;
+            } else {
+                const float2 x = *reinterpret_cast<const float2*>(a);
+                o[0] += wj * x.x;
+                o[1] += wj * x.y;
+            }
         }
     }
 #pragma unroll
-    for (int v = 0; v < V; ++v) part_o[warp][lane * V + v] = o[v];
-    if (lane == 0) part_den[warp] = den;
-    __syncthreads();
-    if (warp == 0) {
-        float d = 0.f;
+    for (int k = 16; k > 0; k >>= 1) den += __shfl_xor_sync(0xffffffffu, den, k);
+    const float inv = 1.f / den;
 #pragma unroll
-        for (int w = 0; w < kReduceWarps; ++w) d += part_den[w];
-        const float inv = 1.f / d;
-        float res[V];
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-            float t = 0.f;
-#pragma unroll
-            for (int w = 0; w < kReduceWarps; ++w) t += part_o[w][lane * V + v];
-            res[v] = t * inv;
-        }
-        store_row<OutT, D>(out + (size_t)r * D, res);
-    }
+    for (int v = 0; v < V; ++v) o[v] *= inv;
+    store_row<OutT, D>(out + (size_t)r * D, o);
 }
 
 template <typename OutT>
 static cudaError_t reduce_dispatch_d(void* out, const float* m2, const float* l, const float* acc,
                                      const int32_t* nparts, int rows_per_seq, int R, int P, int D, bool skip,
                                      int* err, cudaStream_t st) {
-    const dim3 grid(R), block(kReduceWarps * 32);
+    const dim3 grid((R + kReduceWarps - 1) / kReduceWarps), block(kReduceWarps * 32);
     if (D == 128)
         return launch_kernel(partition_reduce_kernel<OutT, 128>, grid, block, 0, st, static_cast<OutT*>(out), m2, l,
                              acc, nparts, rows_per_seq, R, P, skip ? 1 : 0, err);
