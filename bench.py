@@ -375,7 +375,7 @@ def run_ours(args):
     # ---- end-to-end through the public API with host buffers
     e2e_value, h2d, d2h = None, 0, 0
     if not args.no_e2e:
-        e2e_value, h2d, d2h = run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world)
+        e2e_value, h2d, d2h = run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world, tab)
 
     # ---- CPU baseline (rank 0, N = 1 only)
     cpu = None
@@ -409,66 +409,95 @@ def run_ours(args):
     return 0
 
 
-def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world):
-    """Decode steps through the public API from pinned host buffers: host allocation, host->device copies of
-    the step's inputs, cache write, decode, device->host copy of the output, all inside the timed region."""
+def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world, tab):
+    """Decode steps through the public API from pinned host buffers.  Inside the timed region, per step:
+    host block allocation (slots + block-table updates), one host->device copy of the step's inputs
+    (q, new K/V, slots, lengths, table updates), the table update, cache write and decode kernels, and the
+    device->host copy of the output, then a synchronisation.  The allocation of step i+1 depends only on the
+    sequence lengths, so the host runs it while the device executes step i (before that step's sync); the
+    allocation of the first timed step is the warm-up's last overlap."""
     import torch
 
     import paged_kv_cache_302_gb300 as pa
 
-    dt = torch.bfloat16
     e2e_steps = min(args.steps, 30)
     nsteps = e2e_steps + args.warmup
     per_tok = 2 * w.H_kv * w.D * w.elem_bytes
     seq_ids = list(range(w.N))
     ones = np.ones(w.N, dtype=np.int32)
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    e2e_inputs = W.decode_steps(w, nsteps)
-    h_q = [pin(x[0].view(np.int16)) for x in e2e_inputs]
-    h_k = [pin(x[1].view(np.int16)) for x in e2e_inputs]
-    h_v = [pin(x[2].view(np.int16)) for x in e2e_inputs]
+    ctx = np.array([alloc.seq_len(s) for s in seq_ids], dtype=np.int32)
+
+    def al(x):
+        return (x + 15) // 16 * 16
+
+    # staging layout (bytes): q | k | v | slots int64 | ctx int32 | table updates int32[.,3]
+    nq, nk = w.N * w.H_q * w.D * 2, w.N * w.H_kv * w.D * 2
+    o_k = al(nq)
+    o_v = o_k + al(nk)
+    o_s = o_v + al(nk)
+    o_c = o_s + al(w.N * 8)
+    o_u = o_c + al(w.N * 4)
+    total = o_u + al(2 * w.N * 12)
+    stage = []
+    for q, k, v in W.decode_steps(w, nsteps):
+        h = torch.empty(total, dtype=torch.uint8).pin_memory()
+        hb = h.numpy()
+        hb[:nq] = q.view(np.uint8).reshape(-1)
+        hb[o_k:o_k + nk] = k.view(np.uint8).reshape(-1)
+        hb[o_v:o_v + nk] = v.view(np.uint8).reshape(-1)
+        stage.append(h)
+    d_stage = torch.empty(total, dtype=torch.uint8, device=dev)
+    d_q = d_stage[:nq].view(torch.bfloat16).view(w.N, w.H_q, w.D)
+    d_k = d_stage[o_k:o_k + nk].view(torch.bfloat16).view(w.N, w.H_kv, w.D)
+    d_v = d_stage[o_v:o_v + nk].view(torch.bfloat16).view(w.N, w.H_kv, w.D)
+    d_slot = d_stage[o_s:o_s + w.N * 8].view(torch.int64)
+    d_ctx = d_stage[o_c:o_c + w.N * 4].view(torch.int32)
     h_out = torch.empty((w.N, w.H_q, w.D), dtype=torch.float32).pin_memory()
-    h_tab = torch.empty((w.N, MB), dtype=torch.int32).pin_memory()
-    h_ctx = torch.empty(w.N, dtype=torch.int32).pin_memory()
-    h_slot = torch.empty(w.N, dtype=torch.int64).pin_memory()
-    d_q = torch.empty((w.N, w.H_q, w.D), dtype=dt, device=dev)
-    d_k = torch.empty((w.N, w.H_kv, w.D), dtype=dt, device=dev)
-    d_v = torch.empty_like(d_k)
-    d_tab = torch.empty((w.N, MB), dtype=torch.int32, device=dev)
-    d_ctx = torch.empty(w.N, dtype=torch.int32, device=dev)
-    d_slot = torch.empty(w.N, dtype=torch.int64, device=dev)
-    h2d = (h_q[0].numel() * 2 + h_k[0].numel() * 2 * 2 + h_tab.numel() * 4 + h_ctx.numel() * 4 + h_slot.numel() * 8)
     d2h = h_out.numel() * 4
+    h2d_bytes = []
     e2e_bytes = []
 
-    def e2e_step(i):
-        sl, pairs = alloc.append_batch(seq_ids, ones)
-        tbl, cx = alloc.block_tables(seq_ids, MB)
-        h_slot.numpy()[:] = sl
-        h_tab.numpy()[:] = tbl
-        h_ctx.numpy()[:] = cx
-        d_q.view(torch.int16).copy_(h_q[i], non_blocking=True)
-        d_k.view(torch.int16).copy_(h_k[i], non_blocking=True)
-        d_v.view(torch.int16).copy_(h_v[i], non_blocking=True)
-        d_tab.copy_(h_tab, non_blocking=True)
-        d_ctx.copy_(h_ctx, non_blocking=True)
-        d_slot.copy_(h_slot, non_blocking=True)
+    def prepare(i):
+        """Host block allocation of step i into its staging buffer (it needs the lengths only)."""
+        nonlocal ctx
+        sl, pairs, upd = alloc.append_batch(seq_ids, ones, table_updates=True)
+        ctx = ctx + 1
+        hb = stage[i].numpy()
+        hb[o_s:o_s + w.N * 8] = sl.view(np.uint8)
+        hb[o_c:o_c + w.N * 4] = ctx.view(np.uint8)
+        nu = upd.shape[0]
+        hb[o_u:o_u + nu * 12] = np.ascontiguousarray(upd).view(np.uint8).reshape(-1)
+        return nu, pairs, int(ctx.astype(np.int64).sum()) * per_tok
+
+    def e2e_step(i, prep, next_i):
+        """Runs step i; the host prepares step next_i while the device works."""
+        nu, pairs, nbytes = prep
+        used = o_u + nu * 12
+        d_stage[:used].copy_(stage[i][:used], non_blocking=True)
+        if nu:
+            pa.pa_update_block_tables(tab, d_stage[o_u:o_u + nu * 12].view(torch.int32).view(nu, 3), dev_err=err)
         if pairs.size:
             pa.pa_copy_blocks(pool, torch.from_numpy(pairs).to(dev), dev_err=err)
         pa.pa_reshape_and_cache(d_k, d_v, pool, d_slot, dev_err=err)
-        pa.pa_decode(out, d_q, pool, d_tab, d_ctx, max_ctx, partition_tokens=pt, workspace=ws, dev_err=err)
+        pa.pa_decode(out, d_q, pool, tab, d_ctx, max_ctx, partition_tokens=pt, workspace=ws, dev_err=err)
         h_out.copy_(out, non_blocking=True)
+        nxt = prepare(next_i) if next_i is not None else None
         torch.cuda.current_stream().synchronize()
-        return int(cx.astype(np.int64).sum()) * per_tok
+        h2d_bytes.append(used)
+        return nbytes, nxt
 
+    prep = prepare(0)
     for i in range(args.warmup):
-        e2e_step(i)
+        _, prep = e2e_step(i, prep, i + 1)
     if world > 1:
         torch.distributed.barrier()
+    h2d_bytes.clear()
     t0 = time.perf_counter()
     for i in range(args.warmup, nsteps):
-        e2e_bytes.append(e2e_step(i))
+        nbytes, prep = e2e_step(i, prep, i + 1 if i + 1 < nsteps else None)
+        e2e_bytes.append(nbytes)
     t_e2e = time.perf_counter() - t0
+    assert int(err.item()) == 0, f"device error flags {int(err.item())}"
     e2e_value = sum(e2e_bytes) / t_e2e / 1e9
     if world > 1:
         import torch.distributed as dist
@@ -478,7 +507,7 @@ def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world):
         sm = tt[1:].clone()
         dist.all_reduce(sm)
         e2e_value = float(sm.item()) / float(mx.item()) / 1e9
-    return e2e_value, h2d, d2h
+    return e2e_value, int(round(sum(h2d_bytes) / len(h2d_bytes))), d2h
 
 
 def main():

@@ -95,6 +95,20 @@ pa_status pa_copy_blocks(void* pool, const int64_t* pairs, int n, int NB, int B,
                          int* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Incremental block-table update ([VA] 背景と動機: preparing block tables on
+ * the CPU took a large share of a vLLM decode iteration; the tables stay on
+ * the device and only changed entries travel).
+ * tables: [N][MB] int32 device memory; updates: [n][3] int32 device memory
+ * (row, logical block, physical block), as pa_alloc_append_batch emits them.
+ * Sets tables[row][logical block] = physical block.  Entries with row outside
+ * [0, N) or logical block outside [0, MB) are skipped and flagged
+ * PA_DEV_ERR_BLOCK.  Two updates of the same entry race (the allocator never
+ * emits that).  n == 0 is a no-op.
+ * ---------------------------------------------------------------------- */
+pa_status pa_update_block_tables(int32_t* tables, int N, int MB, const int32_t* updates, int n, int* dev_err,
+                                 void* stream);
+
+/* ------------------------------------------------------------------------
  * Workspace for pa_decode / pa_decode_contiguous, in bytes.
  * partition_tokens: 0 = default (512), -1 = one partition per sequence,
  * > 0 = split each context into partitions of that many tokens (a multiple
@@ -209,9 +223,16 @@ pa_status pa_alloc_add_seq(void* alloc, int seq_id);                 /* new empt
 pa_status pa_alloc_append_slots(void* alloc, int seq_id, int n, int64_t* slots_out, int64_t* cow_pairs_out,
                                 int cow_cap, int* n_cow);
 /* Append n_tokens[i] tokens to each of n_seqs distinct sequences, in order.
- * slots_out: [sum n_tokens]; cow_pairs_out: [cow_cap][2]. */
+ * slots_out: [sum n_tokens]; cow_pairs_out: [cow_cap][2].
+ * table_updates_out (nullable): [upd_cap][3] int32 triples (row i of the
+ * batch, logical block, physical block), one per block-table entry the call
+ * sets (each new block and each copy-on-write replacement), in order; *n_upd
+ * receives their count.  Feeding them to pa_update_block_tables keeps a
+ * device copy of the batch's tables ([n_seqs][MB], rows in seq_ids order)
+ * current without re-uploading it. */
 pa_status pa_alloc_append_batch(void* alloc, int n_seqs, const int32_t* seq_ids, const int32_t* n_tokens,
-                                int64_t* slots_out, int64_t* cow_pairs_out, int cow_cap, int* n_cow);
+                                int64_t* slots_out, int64_t* cow_pairs_out, int cow_cap, int* n_cow,
+                                int32_t* table_updates_out, int upd_cap, int* n_upd);
 pa_status pa_alloc_fork(void* alloc, int parent, int child);          /* child shares all parent blocks */
 pa_status pa_alloc_free_seq(void* alloc, int seq_id);                 /* drop references, recycle blocks */
 pa_status pa_alloc_block_table(void* alloc, int seq_id, int32_t* out, int cap, int* n);

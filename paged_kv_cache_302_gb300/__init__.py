@@ -80,7 +80,8 @@ def _declare(L):
         "pa_alloc_destroy": ([P], None),
         "pa_alloc_add_seq": ([P, i32], i32),
         "pa_alloc_append_slots": ([P, i32, i32, P, P, i32, P], i32),
-        "pa_alloc_append_batch": ([P, i32, P, P, P, P, i32, P], i32),
+        "pa_alloc_append_batch": ([P, i32, P, P, P, P, i32, P, P, i32, P], i32),
+        "pa_update_block_tables": ([P, i32, i32, P, i32, P, P], i32),
         "pa_alloc_fork": ([P, i32, i32], i32),
         "pa_alloc_free_seq": ([P, i32], i32),
         "pa_alloc_block_table": ([P, i32, P, i32, P], i32),
@@ -233,6 +234,16 @@ def pa_decode(out, q, pool, block_tables, ctx_lens, max_ctx, scale=None, partiti
     return out
 
 
+def pa_update_block_tables(tables, updates, dev_err=None, stream=None):
+    """Apply (row, logical block, physical block) updates [n, 3] (int32, device) to tables [N, MB]."""
+    N, MB = tables.shape
+    n = updates.shape[0] if updates.numel() else 0
+    L = load()
+    _check(L.pa_update_block_tables(_dev(tables, "tables", torch.int32), N, MB,
+                                    _dev(updates, "updates", torch.int32) if n else None, n, _err_ptr(dev_err),
+                                    _stream_ptr(stream)))
+
+
 PA_STATIC_WORKSPACE_BYTES = 32 * 1024 * 1024
 
 
@@ -348,7 +359,9 @@ class BlockAllocator:
                                              ctypes.byref(ncow)))
         return slots[:n], pairs[: 2 * ncow.value].reshape(-1, 2)
 
-    def append_batch(self, seq_ids, n_tokens):
+    def append_batch(self, seq_ids, n_tokens, table_updates: bool = False):
+        """Append n_tokens[i] tokens to seq_ids[i]; returns (slots, cow_pairs) and, with
+        table_updates=True, also the [k, 3] int32 (row, logical block, physical block) updates."""
         import numpy as np
         ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
         nt = np.ascontiguousarray(n_tokens, dtype=np.int32)
@@ -356,9 +369,15 @@ class BlockAllocator:
         slots = np.zeros(max(total, 1), dtype=np.int64)
         pairs = np.zeros(2 * max(len(ids), 1), dtype=np.int64)
         ncow = ctypes.c_int(0)
+        # entries set per sequence: at most one block per B tokens plus a partial one and a copy
+        cap = int((nt // self.B).sum()) + 2 * len(ids) + 1
+        upd = np.empty((cap, 3), dtype=np.int32) if table_updates else None
+        nupd = ctypes.c_int(0)
         _check(self._L.pa_alloc_append_batch(self._h, len(ids), _i32p(ids), _i32p(nt), _i32p(slots), _i32p(pairs),
-                                             max(len(ids), 1), ctypes.byref(ncow)))
-        return slots[:total], pairs[: 2 * ncow.value].reshape(-1, 2)
+                                             max(len(ids), 1), ctypes.byref(ncow),
+                                             _i32p(upd) if upd is not None else None, cap, ctypes.byref(nupd)))
+        res = (slots[:total], pairs[: 2 * ncow.value].reshape(-1, 2))
+        return res + (upd[: nupd.value],) if table_updates else res
 
     def fork(self, parent: int, child: int):
         _check(self._L.pa_alloc_fork(self._h, int(parent), int(child)))

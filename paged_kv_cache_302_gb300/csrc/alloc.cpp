@@ -46,8 +46,11 @@ static int64_t blocks_needed(const Allocator& A, const Seq& s, int64_t n, int la
     return need + (want - have);
 }
 
-// Applies an append whose block demand has been checked.
-static void apply_append(Allocator& A, Seq& s, int64_t n, int64_t* slots, std::vector<int64_t>& cow) {
+// Applies an append whose block demand has been checked.  Every table entry
+// the append sets (a new block, or the copy that replaces a shared one) is
+// recorded in `upd` as (row, logical block, physical block) when upd != NULL.
+static void apply_append(Allocator& A, Seq& s, int64_t n, int64_t* slots, std::vector<int64_t>& cow,
+                         std::vector<int32_t>* upd = nullptr, int row = 0) {
     for (int64_t i = 0; i < n; ++i) {
         const int64_t pos = s.ntok;
         const int64_t off = pos % A.B;
@@ -56,6 +59,7 @@ static void apply_append(Allocator& A, Seq& s, int64_t n, int64_t* slots, std::v
             A.free_stack.pop_back();
             A.ref[b] = 1;
             s.blocks.push_back(b);
+            if (upd) upd->insert(upd->end(), {row, (int32_t)(pos / A.B), b});
         } else if (A.ref[s.blocks.back()] > 1) {
             const int32_t old = s.blocks.back();
             const int32_t b = A.free_stack.back();
@@ -65,6 +69,7 @@ static void apply_append(Allocator& A, Seq& s, int64_t n, int64_t* slots, std::v
             s.blocks.back() = b;
             cow.push_back(old);
             cow.push_back(b);
+            if (upd) upd->insert(upd->end(), {row, (int32_t)(pos / A.B), b});
         }
         slots[i] = (int64_t)s.blocks[pos / A.B] * A.B + off;
         s.ntok = pos + 1;
@@ -139,7 +144,8 @@ pa_status pa_alloc_append_slots(void* alloc, int seq_id, int n, int64_t* slots_o
 }
 
 pa_status pa_alloc_append_batch(void* alloc, int n_seqs, const int32_t* seq_ids, const int32_t* n_tokens,
-                                int64_t* slots_out, int64_t* cow_pairs_out, int cow_cap, int* n_cow) {
+                                int64_t* slots_out, int64_t* cow_pairs_out, int cow_cap, int* n_cow,
+                                int32_t* table_updates_out, int upd_cap, int* n_upd) {
     Allocator* A = as_alloc(alloc);
     if (!A) return fail(PA_ERR_INVALID, "null allocator");
     if (n_seqs < 0) return fail(PA_ERR_INVALID, "negative n_seqs");
@@ -170,14 +176,21 @@ pa_status pa_alloc_append_batch(void* alloc, int n_seqs, const int32_t* seq_ids,
     if (copies > 0 && (cow_cap < copies || !cow_pairs_out)) return fail(PA_ERR_INVALID, "cow_pairs_out too small");
     if (need > (int64_t)A->free_stack.size())
         return fail(PA_ERR_OOM, "need %lld blocks, %zu free", (long long)need, A->free_stack.size());
+    // every table entry set by the batch is a block taken from the free list
+    if (table_updates_out && need > upd_cap)
+        return fail(PA_ERR_INVALID, "table_updates_out holds %d entries, the batch sets %lld", upd_cap,
+                    (long long)need);
     std::vector<int64_t> cow;
+    std::vector<int32_t> upd;
     int64_t off = 0;
     for (int i = 0; i < n_seqs; ++i) {
-        apply_append(*A, *seqs[i], n_tokens[i], slots_out + off, cow);
+        apply_append(*A, *seqs[i], n_tokens[i], slots_out + off, cow, table_updates_out ? &upd : nullptr, i);
         off += n_tokens[i];
     }
     for (size_t i = 0; i < cow.size(); ++i) cow_pairs_out[i] = cow[i];
     if (n_cow) *n_cow = (int)(cow.size() / 2);
+    if (table_updates_out && !upd.empty()) std::memcpy(table_updates_out, upd.data(), upd.size() * sizeof(int32_t));
+    if (n_upd) *n_upd = (int)(upd.size() / 3);
     return PA_OK;
 }
 

@@ -106,4 +106,28 @@ pa_status launch_copy_blocks(void* pool, const int64_t* pairs, int n, int NB, in
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "copy_blocks launch");
 }
 
+// One thread per table update (row, logical block, physical block).
+__global__ void __launch_bounds__(256) update_tables_kernel(int32_t* __restrict__ tables, int N, int MB,
+                                                            const int3* __restrict__ upd, int n, int* err) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int3 u = upd[i];
+    if (u.x < 0 || u.x >= N || u.y < 0 || u.y >= MB) {
+        flag_error(err, PA_DEV_ERR_BLOCK);
+        return;
+    }
+    tables[(size_t)u.x * MB + u.y] = u.z;
+}
+
+pa_status launch_update_tables(int32_t* tables, int N, int MB, const int32_t* updates, int n, int* dev_err,
+                               cudaStream_t stream) {
+    if (n == 0) return PA_OK;
+    cudaError_t e = launch_kernel(update_tables_kernel, dim3((n + 255) / 256), dim3(256), 0, stream, tables, N, MB,
+                                  reinterpret_cast<const int3*>(updates), n, dev_err);
+    count_launch();
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "update_block_tables launch");
+}
+
 }  // namespace pa

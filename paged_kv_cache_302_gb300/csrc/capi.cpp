@@ -99,6 +99,17 @@ pa_status pa_copy_blocks(void* pool, const int64_t* pairs, int n, int NB, int B,
     return launch_copy_blocks(pool, pairs, n, NB, B, H_kv, D, dev_err, static_cast<cudaStream_t>(stream));
 }
 
+pa_status pa_update_block_tables(int32_t* tables, int N, int MB, const int32_t* updates, int n, int* dev_err,
+                                 void* stream) {
+    g_msg[0] = 0;
+    if (N <= 0 || MB <= 0 || n < 0) return fail(PA_ERR_INVALID, "bad sizes");
+    if (n == 0) return PA_OK;
+    if (!tables || !updates) return fail(PA_ERR_INVALID, "null pointer argument");
+    if ((reinterpret_cast<uintptr_t>(updates) & 3u) || (reinterpret_cast<uintptr_t>(tables) & 3u))
+        return fail(PA_ERR_INVALID, "tables and updates must be 4-byte aligned");
+    return launch_update_tables(tables, N, MB, updates, n, dev_err, static_cast<cudaStream_t>(stream));
+}
+
 size_t pa_decode_workspace_bytes(int N, int H_q, int H_kv, int D, int max_ctx, int partition_tokens) {
     WorkspaceLayout L;
     if (!workspace_layout(N, H_q, H_kv, D, max_ctx, partition_tokens, &L)) return 0;

@@ -81,23 +81,29 @@ def _run_same_ops(NB, B, order, ops):
                 assert [tuple(r) for r in got[1]] == want[1]
         elif kind == "batch":
             try:
-                got = cpp.append_batch(op[1], op[2])
+                got = cpp.append_batch(op[1], op[2], table_updates=True)
             except pa.PAError as e:
                 got_err, got = e.status, None
             snapshot = (list(ref.free), list(ref.ref), {k: list(v) for k, v in ref.tables.items()}, dict(ref.ntok))
             try:
-                slots, pairs = [], []
-                for s, n in zip(op[1], op[2]):
+                slots, pairs, upd = [], [], []
+                for row, (s, n) in enumerate(zip(op[1], op[2])):
+                    before = list(ref.tables[s]) if s in ref.tables else []
                     a, b = ref.append_slots(s, n)
                     slots += a
                     pairs += b
-                want = (slots, pairs)
+                    after = ref.tables[s]
+                    # table entries that changed or appeared, in logical order
+                    upd += [(row, lb, after[lb]) for lb in range(len(after))
+                            if lb >= len(before) or before[lb] != after[lb]]
+                want = (slots, pairs, upd)
             except AllocError as e:
                 want_err, want = e.kind, None
                 ref.free, ref.ref, ref.tables, ref.ntok = snapshot      # the batch is all-or-nothing
             if got is not None and want is not None:
                 assert list(got[0]) == want[0]
                 assert [tuple(r) for r in got[1]] == want[1]
+                assert [tuple(int(x) for x in r) for r in got[2]] == want[2]
         elif kind == "fork":
             try:
                 cpp.fork(op[1], op[2])

@@ -65,6 +65,37 @@ def test_copy_blocks_bit_exact_and_flags():
     assert err.item() & pa.PA_DEV_ERR_BLOCK
 
 
+def test_table_updates_keep_the_device_tables_current():
+    """Device tables patched with the allocator's updates equal freshly packed host tables, bit for bit."""
+    w = W.cow(prompts=4, samples=8)
+    a = pa.BlockAllocator(w.NB, w.B, w.free_order)
+    for p in range(w.prompts):
+        a.add_seq(p * w.samples)
+        a.append_slots(p * w.samples, w.prompt_len)
+        for j in range(1, w.samples):
+            a.fork(p * w.samples, p * w.samples + j)
+    order = list(np.random.default_rng(5).permutation(w.N))   # device rows in an arbitrary sequence order
+    MB = w.max_blocks_per_seq(grow=64)
+    tab0, _ = a.block_tables(order, MB)
+    dev = torch.from_numpy(tab0).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rng = np.random.default_rng(6)
+    for step in range(6):
+        n_tok = rng.integers(0, 40, size=w.N).astype(np.int32)     # first step: copy-on-write for 7 of 8 samples
+        _, pairs, upd = a.append_batch(order, n_tok, table_updates=True)
+        if step == 0:
+            assert len(pairs) > 0
+        pa.pa_update_block_tables(dev, torch.from_numpy(np.ascontiguousarray(upd)).cuda(), dev_err=err)
+        want, _ = a.block_tables(order, MB)
+        torch.cuda.synchronize()
+        assert np.array_equal(dev.cpu().numpy(), want) and err.item() == 0
+    bad = torch.tensor([[w.N, 0, 1], [0, MB, 1]], dtype=torch.int32, device="cuda")
+    pa.pa_update_block_tables(dev, bad, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() & pa.PA_DEV_ERR_BLOCK
+    assert np.array_equal(dev.cpu().numpy(), want)
+
+
 # ----------------------------------------------------------------------------- decode, every output
 
 def test_tiny_worked_example_every_output():
