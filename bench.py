@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--seqs", type=int, default=256,
                     help="sequences (256 is the benchmarked workload; fewer for small profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--measure", choices=["decode", "swap"], default="decode",
+                    help="swap: time pa_swap_blocks device<->pinned host instead of the decode step")
     return ap.parse_args()
 
 
@@ -510,10 +512,57 @@ def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world, tab
     return e2e_value, int(round(sum(h2d_bytes) / len(h2d_bytes))), d2h
 
 
+def run_swap(args):
+    """Swap bandwidth: pa_swap_blocks moving whole Llama-3-8B-shaped blocks (16 tokens x 8 KV heads x 128, bf16:
+    64 KB each) between the device pool and a pinned host pool, both directions, CUDA events."""
+    import torch
+
+    import paged_kv_cache_302_gb300 as pa
+
+    torch.cuda.set_device(0)
+    B, H, D, nblk = 16, 8, 128, 4096            # 256 MB per direction
+    dev_pool = torch.empty((nblk, B, 2, H, D), dtype=torch.bfloat16, device="cuda").normal_()
+    host_pool = torch.empty((nblk, B, 2, H, D), dtype=torch.bfloat16).pin_memory()
+    rng = np.random.default_rng(12)
+    out_pairs = torch.from_numpy(np.stack([rng.permutation(nblk), rng.permutation(nblk)], 1).astype(np.int64)).cuda()
+    in_pairs = torch.from_numpy(np.stack([rng.permutation(nblk), rng.permutation(nblk)], 1).astype(np.int64)).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    res = {}
+    for name, dst, src, pairs in (("swap_out_d2h", host_pool, dev_pool, out_pairs),
+                                  ("swap_in_h2d", dev_pool, host_pool, in_pairs)):
+        for _ in range(args.warmup):
+            pa.pa_swap_blocks(dst, src, pairs, dev_err=err)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            pa.pa_swap_blocks(dst, src, pairs, dev_err=err)
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) * 1e-3 / args.steps
+        res[name] = dev_pool.numel() * 2 / t / 1e9
+    # copy-engine reference: one contiguous cudaMemcpy of the same bytes each way
+    for name, dst, src in (("memcpy_d2h_contiguous", host_pool, dev_pool), ("memcpy_h2d_contiguous", dev_pool,
+                                                                             host_pool)):
+        dst.copy_(src, non_blocking=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = dev_pool.numel() * 2 / (e0.elapsed_time(e1) * 1e-3 / args.steps) / 1e9
+    assert int(err.item()) == 0
+    print(json.dumps({"measure": "pa_swap_blocks", "unit": "GB/s", "blocks": nblk, "block_bytes": B * 2 * H * D * 2,
+                      "steps": args.steps, **res}), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.measure == "swap":
+        return run_swap(args)
     return run_ours(args)
 
 

@@ -95,6 +95,24 @@ pa_status pa_copy_blocks(void* pool, const int64_t* pairs, int n, int NB, int B,
                          int* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Block swap between two pools ([PA] 実装のポイント: under memory pressure the
+ * scheduler preempts a request and either swaps its KV cache to CPU memory
+ * or recomputes it later; this is the swap copy, in both directions).
+ * dst_pool: [NB_dst][B][2][H_kv][D], src_pool: [NB_src][B][2][H_kv][D]; each
+ * is device memory or page-locked host memory (cudaHostAlloc, or pinned with
+ * cudaHostRegister; with unified addressing its host pointer is used as is).
+ * Pageable host memory is rejected with PA_ERR_INVALID.
+ * pairs: [n][2] int64 (src block, dst block), in device or page-locked host
+ * memory.  dst_pool[dst] = src_pool[src] for whole blocks, bit for bit, moved
+ * by the GPU's own loads and stores (no per-block memcpy calls).  A pair
+ * outside [0, NB_src) x [0, NB_dst) is skipped and flagged PA_DEV_ERR_BLOCK;
+ * destinations must be distinct.  For copies inside one pool use
+ * pa_copy_blocks.  n == 0 is a no-op.
+ * ---------------------------------------------------------------------- */
+pa_status pa_swap_blocks(void* dst_pool, int NB_dst, const void* src_pool, int NB_src, const int64_t* pairs, int n,
+                         int B, int H_kv, int D, pa_dtype dtype, int* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
  * Incremental block-table update ([VA] 背景と動機: preparing block tables on
  * the CPU took a large share of a vLLM decode iteration; the tables stay on
  * the device and only changed entries travel).

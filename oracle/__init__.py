@@ -67,6 +67,7 @@ def lib():
             L.oracle_tokens_per_page.restype = dbl
             L.oracle_reshape_and_cache.argtypes = [P, P, P, P, i32, i32, i32, i32, i32]
             L.oracle_copy_blocks.argtypes = [P, P, i32, i32, i32, i32, i32]
+            L.oracle_swap_blocks.argtypes = [P, i32, P, i32, P, i32, ctypes.c_int64]
             L.oracle_paged_decode.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, dbl, i32, P, i32, i32]
             L.oracle_contiguous_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, dbl, i32, P, i32,
                                                    i32]
@@ -74,7 +75,7 @@ def lib():
             L.oracle_paged_partials_row.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, dbl, i32, i32, i32]
             L.oracle_partition_merge.argtypes = [P, P, P, P, P, i32, i32, i32]
             L.oracle_num_threads.argtypes = []
-            for name in ("oracle_reshape_and_cache", "oracle_copy_blocks", "oracle_paged_decode",
+            for name in ("oracle_reshape_and_cache", "oracle_copy_blocks", "oracle_swap_blocks", "oracle_paged_decode",
                          "oracle_contiguous_decode", "oracle_paged_decode_online_row", "oracle_paged_partials_row",
                          "oracle_partition_merge", "oracle_num_threads"):
                 getattr(L, name).restype = i32
@@ -147,6 +148,17 @@ def copy_blocks(pool, pairs):
     pr = _c(pairs, np.int64).reshape(-1, 2)
     NB, B, _, H_kv, D = pool.shape
     _check(lib().oracle_copy_blocks(_ptr(pool), _ptr(pr), pr.shape[0], NB, B, H_kv, D), "copy_blocks")
+
+
+def swap_blocks(dst_pool, src_pool, pairs):
+    """dst_pool[dst] = src_pool[src] for each (src, dst) row of ``pairs`` (in place on dst_pool)."""
+    assert dst_pool.flags.c_contiguous and dst_pool.dtype == np.uint16 and src_pool.dtype == np.uint16
+    assert dst_pool.shape[1:] == src_pool.shape[1:]
+    src_pool = _c(src_pool, np.uint16)
+    pr = _c(pairs, np.int64).reshape(-1, 2)
+    blk = int(np.prod(dst_pool.shape[1:]))
+    _check(lib().oracle_swap_blocks(_ptr(dst_pool), dst_pool.shape[0], _ptr(src_pool), src_pool.shape[0], _ptr(pr),
+                                    pr.shape[0], blk), "swap_blocks")
 
 
 # --------------------------------------------------------------------------- attention

@@ -124,6 +124,26 @@ int oracle_copy_blocks(uint16_t* pool, const int64_t* pairs, int n, int NB, int 
 }
 
 /* ---------------------------------------------------------------------------
+ * Swap copy between two pools ([PA] 実装のポイント: a preempted request's KV
+ * cache is moved to CPU memory and back).  pairs: [n][2] = (src block in
+ * src_pool, dst block in dst_pool); whole blocks of blk_elems elements.
+ * ------------------------------------------------------------------------- */
+int oracle_swap_blocks(uint16_t* dst_pool, int NB_dst, const uint16_t* src_pool, int NB_src, const int64_t* pairs,
+                       int n, int64_t blk_elems) {
+    if (n < 0 || blk_elems <= 0) return ORC_INVALID;
+    for (int i = 0; i < n; ++i) {
+        int64_t s = pairs[2 * i], d = pairs[2 * i + 1];
+        if (s < 0 || s >= NB_src || d < 0 || d >= NB_dst) return ORC_INVALID;
+        for (int j = 0; j < i; ++j)
+            if (pairs[2 * j + 1] == d) return ORC_INVALID; /* destinations are distinct */
+    }
+    for (int i = 0; i < n; ++i)
+        memcpy(dst_pool + pairs[2 * i + 1] * blk_elems, src_pool + pairs[2 * i] * blk_elems,
+               (size_t)blk_elems * sizeof(uint16_t));
+    return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------------
  * Decode attention, plain definition ([PA] 技術的詳細 / PagedAttentionアルゴリズム,
  * decode equation for o_t):  for query q of head h,
  *     x_t = (q . K_t) * scale,   o = sum_t softmax(x)_t V_t,   t = 0 .. ctx-1,

@@ -82,6 +82,7 @@ def _declare(L):
         "pa_alloc_append_slots": ([P, i32, i32, P, P, i32, P], i32),
         "pa_alloc_append_batch": ([P, i32, P, P, P, P, i32, P, P, i32, P], i32),
         "pa_update_block_tables": ([P, i32, i32, P, i32, P, P], i32),
+        "pa_swap_blocks": ([P, i32, P, i32, P, i32, i32, i32, i32, i32, P, P], i32),
         "pa_alloc_fork": ([P, i32, i32], i32),
         "pa_alloc_free_seq": ([P, i32], i32),
         "pa_alloc_block_table": ([P, i32, P, i32, P], i32),
@@ -232,6 +233,31 @@ def pa_decode(out, q, pool, block_tables, ctx_lens, max_ctx, scale=None, partiti
                        ws.numel() * ws.element_size(), _dtype_code(pool.dtype), _err_ptr(dev_err),
                        _events_arg(attend_events, stream), _stream_ptr(stream)))
     return out
+
+
+def _acc(t: torch.Tensor, name: str):
+    """Pointer of a tensor the GPU can address: a CUDA tensor or a pinned host tensor."""
+    if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+        raise PAError(PA_ERR_INVALID, f"{name} must be a contiguous tensor")
+    if not t.is_cuda and not t.is_pinned():
+        raise PAError(PA_ERR_INVALID, f"{name} must be on a CUDA device or in pinned host memory")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def pa_swap_blocks(dst_pool, src_pool, pairs, dev_err=None, stream=None):
+    """dst_pool[dst] = src_pool[src] for (src, dst) rows of pairs [n, 2] int64; pools [NB, B, 2, H_kv, D] on the
+    device or in pinned host memory (swap out: device -> host, swap in: host -> device)."""
+    NBd, B, _, H_kv, D = dst_pool.shape
+    NBs = src_pool.shape[0]
+    if tuple(src_pool.shape[1:]) != tuple(dst_pool.shape[1:]) or src_pool.dtype != dst_pool.dtype:
+        raise PAError(PA_ERR_INVALID, "pools differ in block shape or dtype")
+    if pairs.dtype != torch.int64:
+        raise PAError(PA_ERR_INVALID, "pairs must be int64")
+    n = pairs.shape[0] if pairs.numel() else 0
+    L = load()
+    _check(L.pa_swap_blocks(_acc(dst_pool, "dst_pool"), NBd, _acc(src_pool, "src_pool"), NBs,
+                            _acc(pairs, "pairs") if n else None, n, B, H_kv, D, _dtype_code(dst_pool.dtype),
+                            _err_ptr(dev_err), _stream_ptr(stream)))
 
 
 def pa_update_block_tables(tables, updates, dev_err=None, stream=None):

@@ -130,4 +130,50 @@ pa_status launch_update_tables(int32_t* tables, int N, int MB, const int32_t* up
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "update_block_tables launch");
 }
 
+// Swap copy between two pools (either may be page-locked host memory): one CTA
+// row per pair, grid.y chunks of the block, kCopyUnroll loads in flight per thread.
+__global__ void __launch_bounds__(kCopyThreads) swap_blocks_kernel(uint4* __restrict__ dst,
+                                                                   const uint4* __restrict__ src,
+                                                                   const int64_t* __restrict__ pairs, int NB_dst,
+                                                                   int NB_src, int64_t blk_vec, int* err) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int i = blockIdx.x;
+    const int64_t s = pairs[2 * i], d = pairs[2 * i + 1];
+    if (s < 0 || s >= NB_src || d < 0 || d >= NB_dst) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) flag_error(err, PA_DEV_ERR_BLOCK);
+        return;
+    }
+    const uint4* sp = src + s * blk_vec;
+    uint4* dp = dst + d * blk_vec;
+    const int64_t chunk = (int64_t)kCopyThreads * kCopyUnroll;
+    for (int64_t base = (int64_t)blockIdx.y * chunk; base < blk_vec; base += (int64_t)gridDim.y * chunk) {
+        uint4 r[kCopyUnroll];
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+            const int64_t e = base + u * kCopyThreads + threadIdx.x;
+            if (e < blk_vec) r[u] = sp[e];
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+            const int64_t e = base + u * kCopyThreads + threadIdx.x;
+            if (e < blk_vec) dp[e] = r[u];
+        }
+    }
+}
+
+pa_status launch_swap_blocks(void* dst, int NB_dst, const void* src, int NB_src, const int64_t* pairs, int n,
+                             int64_t blk_bytes, int* dev_err, cudaStream_t stream) {
+    if (n == 0) return PA_OK;
+    const int64_t blk_vec = blk_bytes / 16;
+    const int64_t chunk = (int64_t)kCopyThreads * kCopyUnroll;
+    int64_t gy = (blk_vec + chunk - 1) / chunk;
+    if (gy > 65535) gy = 65535;
+    cudaError_t e = launch_kernel(swap_blocks_kernel, dim3(n, (unsigned)gy), dim3(kCopyThreads), 0, stream,
+                                  static_cast<uint4*>(dst), static_cast<const uint4*>(src), pairs, NB_dst, NB_src,
+                                  blk_vec, dev_err);
+    count_launch();
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "swap_blocks launch");
+}
+
 }  // namespace pa

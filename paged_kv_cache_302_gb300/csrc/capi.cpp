@@ -99,6 +99,37 @@ pa_status pa_copy_blocks(void* pool, const int64_t* pairs, int n, int NB, int B,
     return launch_copy_blocks(pool, pairs, n, NB, B, H_kv, D, dev_err, static_cast<cudaStream_t>(stream));
 }
 
+// A pointer the GPU may dereference: device memory, managed memory, or page-locked host memory.
+static pa_status check_device_accessible(const void* p, const char* what) {
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
+    if (attr.type == cudaMemoryTypeUnregistered)
+        return fail(PA_ERR_INVALID, "%s is pageable host memory; pin it (cudaHostAlloc / cudaHostRegister)", what);
+    if (attr.type == cudaMemoryTypeHost && !attr.devicePointer)
+        return fail(PA_ERR_INVALID, "%s is page-locked but not mapped into the device address space", what);
+    return PA_OK;
+}
+
+pa_status pa_swap_blocks(void* dst_pool, int NB_dst, const void* src_pool, int NB_src, const int64_t* pairs, int n,
+                         int B, int H_kv, int D, pa_dtype dtype, int* dev_err, void* stream) {
+    g_msg[0] = 0;
+    if (!kv_dtype_ok(dtype)) return fail(PA_ERR_UNSUPPORTED, "dtype must be F16 or BF16");
+    if (n < 0 || NB_dst <= 0 || NB_src <= 0 || B <= 0 || H_kv <= 0 || D <= 0) return fail(PA_ERR_INVALID, "bad sizes");
+    const long long blk_bytes = (long long)B * 2 * H_kv * D * 2;
+    if (blk_bytes % 16) return fail(PA_ERR_UNSUPPORTED, "block bytes must be a multiple of 16");
+    if (n > (1 << 30)) return fail(PA_ERR_INVALID, "too many pairs");
+    if (n == 0) return PA_OK;
+    if (!dst_pool || !src_pool || !pairs) return fail(PA_ERR_INVALID, "null pointer argument");
+    if (!aligned16(dst_pool) || !aligned16(src_pool)) return fail(PA_ERR_INVALID, "pools must be 16-byte aligned");
+    pa_status st = check_device_accessible(dst_pool, "dst_pool");
+    if (st == PA_OK) st = check_device_accessible(src_pool, "src_pool");
+    if (st == PA_OK) st = check_device_accessible(pairs, "pairs");
+    if (st != PA_OK) return st;
+    return launch_swap_blocks(dst_pool, NB_dst, src_pool, NB_src, pairs, n, blk_bytes, dev_err,
+                              static_cast<cudaStream_t>(stream));
+}
+
 pa_status pa_update_block_tables(int32_t* tables, int N, int MB, const int32_t* updates, int n, int* dev_err,
                                  void* stream) {
     g_msg[0] = 0;

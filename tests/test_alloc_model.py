@@ -162,3 +162,44 @@ def test_errors():
         m.fork(1, 2)
     with pytest.raises(AllocError):
         AllocModel(3, 4, [0, 0, 1])
+
+
+def _apply(m, op):
+    kind = op[0]
+    if kind == "add":
+        m.add_seq(op[1])
+    elif kind == "append":
+        return m.append_slots(op[1], op[2])
+    elif kind == "fork":
+        m.fork(op[1], op[2])
+    elif kind == "free":
+        m.free_seq(op[1])
+    return None
+
+
+def test_beam_search_fork_tree_shares_prefixes_and_copies_on_write():
+    """Beams forked from beams share every common prefix block; each shared block's count equals the
+    number of live beams whose table holds it, and a write never lands in a block another beam reads."""
+    ops = W.beam_search_ops()
+    m = AllocModel(256, 16, np.random.default_rng(7).permutation(256))
+    copies = 0
+    for op in ops:
+        if op[0] == "round_end":
+            live = op[1]
+            holders = {}
+            for b in live:
+                for blk in m.block_table(b):
+                    holders[blk] = holders.get(blk, 0) + 1
+            assert all(m.refcount(blk) == n for blk, n in holders.items())
+            assert len(m.tables) == len(live)
+            # the prompt's first full block is shared by every live beam
+            assert holders[m.block_table(live[0])[0]] == len(live)
+            _invariants(m)
+            continue
+        res = _apply(m, op)
+        if res is not None:
+            slots, cow = res
+            copies += len(cow)
+            for s in slots:
+                assert m.refcount(s // m.B) == 1
+    assert copies > 0

@@ -218,3 +218,16 @@ def test_block_tables_packing():
     assert list(tab[2]) == [2, 3, 4, -1]
     with pytest.raises(pa.PAError):
         a.block_tables([1], 2)
+
+
+def test_allocator_matches_model_on_beam_search_fork_tree():
+    ops = [o for o in W.beam_search_ops() if o[0] != "round_end"]
+    _run_same_ops(256, 16, np.random.default_rng(7).permutation(256), ops)
+
+
+def test_swap_rejects_pageable_host_memory_before_any_launch():
+    L = pa.load()
+    host = np.zeros((4, 16, 2, 1, 64), dtype=np.uint16)
+    pairs = np.zeros((1, 2), dtype=np.int64)
+    st = L.pa_swap_blocks(host.ctypes.data, 4, host.ctypes.data, 4, pairs.ctypes.data, 1, 16, 1, 64, 1, None, None)
+    assert st in (pa.PA_ERR_INVALID, pa.PA_ERR_CUDA)

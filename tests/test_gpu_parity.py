@@ -276,3 +276,92 @@ def test_full_cow_parallel_sampling():
 @pytest.mark.parametrize("B", [8, 16, 32])
 def test_full_yi34b_long_context(B):
     _full_check(C.build_paged(W.yi34b_long(B=B), check_pool=(B == 16)), n_pairs=16)
+
+
+# ----------------------------------------------------------------------------- swap and beam search
+
+def test_swap_out_and_back_in_is_bit_exact_and_decodes_identically():
+    w = W.llama3_8b(n_seqs=8, grow=8192)        # enough spare blocks to move the longest sequence
+    c = C.build_paged(w, check_pool=False)
+    rng = np.random.default_rng(8)
+    s = int(np.argmax(w.ctx))
+    nb = -(-int(w.ctx[s]) // w.B)
+    blocks = c.tables[s, :nb].astype(np.int64)
+    NBh = nb + 40
+    host_pool = torch.zeros((NBh, w.B, 2, w.H_kv, w.D), dtype=torch.bfloat16).pin_memory()
+    host_ids = rng.choice(NBh, size=nb, replace=False).astype(np.int64)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out_pairs = torch.from_numpy(np.stack([blocks, host_ids], axis=1)).cuda()          # swap out: device -> host
+    pa.pa_swap_blocks(host_pool, c.pool, out_pairs, dev_err=err)
+    torch.cuda.synchronize()
+    dev_bits = C.to_bits(c.pool)
+    want = np.zeros(host_pool.shape, dtype=np.uint16)
+    oracle.swap_blocks(want, dev_bits, np.stack([blocks, host_ids], axis=1))
+    assert np.array_equal(host_pool.view(torch.int16).numpy().view(np.uint16), want) and err.item() == 0
+    used = set(c.tables[c.tables >= 0].tolist())
+    free = np.array([b for b in range(w.NB) if b not in used][:nb], dtype=np.int64)
+    in_pairs = torch.from_numpy(np.stack([host_ids, free], axis=1)).pin_memory()       # swap in: host -> device,
+    pa.pa_swap_blocks(c.pool, host_pool, in_pairs, dev_err=err)                        # pairs in pinned memory
+    torch.cuda.synchronize()
+    oracle.swap_blocks(dev_bits, want, np.stack([host_ids, free], axis=1))
+    assert np.array_equal(C.to_bits(c.pool), dev_bits) and err.item() == 0
+    ref = C.gpu_decode(c)
+    moved = c.tables.copy()
+    moved[s, :nb] = free
+    got = C.gpu_decode(C.Paged(w, c.pool, None, moved, c.ctx, c.q))
+    assert torch.equal(ref, got)
+    bad = torch.tensor([[0, NBh]], dtype=torch.int64, device="cuda")
+    pa.pa_swap_blocks(host_pool, c.pool, bad, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() & pa.PA_DEV_ERR_BLOCK
+    with pytest.raises(pa.PAError):
+        pa.pa_swap_blocks(torch.zeros_like(host_pool, device="cpu"), c.pool, out_pairs)   # pageable: refused
+
+
+def test_beam_search_fork_tree_decode_every_output():
+    """Beams forked from beams: copy-on-write pairs copied on the device before the writes, then every
+    live beam decoded; pool bit-exact and outputs against the oracle."""
+    from oracle.alloc_model import AllocModel
+    shape = W.llama3_8b(n_seqs=1)
+    NB, B = 256, 16
+    order = np.random.default_rng(7).permutation(NB)
+    a = pa.BlockAllocator(NB, B, order)
+    m = AllocModel(NB, B, order)
+    pool = torch.empty((NB, B, 2, shape.H_kv, shape.D), dtype=torch.bfloat16, device="cuda")
+    pool.view(torch.int16).fill_(C.nan16("bf16"))
+    host = np.full(pool.shape, W.NAN_BITS["bf16"], dtype=np.uint16)
+    rng = np.random.default_rng(9)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    live = []
+    for op in W.beam_search_ops():
+        kind = op[0]
+        if kind == "add":
+            a.add_seq(op[1]); m.add_seq(op[1])
+        elif kind == "fork":
+            a.fork(op[1], op[2]); m.fork(op[1], op[2])
+        elif kind == "free":
+            a.free_seq(op[1]); m.free_seq(op[1])
+        elif kind == "append":
+            slots, pairs = a.append_slots(op[1], op[2])
+            ms, mp = m.append_slots(op[1], op[2])
+            assert list(slots) == ms and [tuple(r) for r in pairs] == mp
+            if len(mp):
+                pa.pa_copy_blocks(pool, torch.from_numpy(np.ascontiguousarray(pairs)).cuda(), dev_err=err)
+                oracle.copy_blocks(host, np.asarray(mp, dtype=np.int64))
+            k = W.normal_bits(rng, (op[2], shape.H_kv, shape.D), "bf16")
+            v = W.normal_bits(rng, (op[2], shape.H_kv, shape.D), "bf16")
+            pa.pa_reshape_and_cache(C.to_dev(k, "bf16"), C.to_dev(v, "bf16"), pool, torch.from_numpy(slots).cuda(),
+                                    dev_err=err)
+            oracle.reshape_and_cache(k, v, host, np.asarray(ms, dtype=np.int64))
+        else:
+            live = list(op[1])
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert np.array_equal(C.to_bits(pool), host)
+    MB = 8
+    tables, ctx = a.block_tables(live, MB)
+    q = W.normal_bits(rng, (len(live), shape.H_q, shape.D), "bf16")
+    wl = W.Workload("beams", 0, len(live), shape.H_q, shape.H_kv, shape.D, B, "bf16", ctx, NB, order)
+    c = C.Paged(wl, pool, host, tables, ctx, q)
+    for pt in (0, -1, 32):
+        C.assert_close(C.gpu_decode(c, partition_tokens=pt).cpu().numpy(), C.oracle_decode(c), f"beams pt={pt}")

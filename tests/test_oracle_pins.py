@@ -347,3 +347,18 @@ def test_rows_listed_twice_are_computed_correctly_in_parallel():
     for _ in range(5):
         sub = oracle.paged_decode(q, pool, tables, ctx, "bf16", pairs=pairs, nthreads=8)
         assert np.array_equal(sub[0, 1], full[0, 1]) and np.array_equal(sub[1, 0], full[1, 0])
+
+
+def test_swap_blocks_matches_numpy_copy_between_pools():
+    rng = np.random.default_rng(34)
+    dev = W.normal_bits(rng, (12, 4, 2, 2, 16), "bf16")
+    host = W.normal_bits(rng, (7, 4, 2, 2, 16), "bf16")
+    ref = host.copy()
+    pairs = np.array([[3, 6], [11, 0], [3, 2]], dtype=np.int64)
+    oracle.swap_blocks(host, dev, pairs)
+    for s, d in pairs:
+        ref[d] = dev[s]
+    assert np.array_equal(host, ref)
+    for bad in ([[0, 7]], [[12, 0]], [[1, 2], [3, 2]]):
+        with pytest.raises(oracle.OracleError):
+            oracle.swap_blocks(host, dev, np.array(bad, dtype=np.int64))

@@ -195,3 +195,35 @@ def decode_steps(w: Workload, steps: int):
 
 def by_name(name: str, **kw) -> Workload:
     return {"tiny": tiny, "opt13b": opt13b, "llama3_8b": llama3_8b, "cow": cow, "yi34b_long": yi34b_long}[name](**kw)
+
+
+def beam_search_ops(seed: int = SEED_BASE + 5, prompt_len: int = 37, beams: int = 4, rounds: int = 6,
+                    tokens_per_round=(1, 5)):
+    """A seeded beam-search schedule as allocator operations.
+
+    Start: one prompt sequence (id 0) of `prompt_len` tokens, forked into `beams` beams.  Each round every live
+    beam appends U{tokens_per_round} tokens; then the lowest-ranked half of the beams (a seeded choice) is freed
+    and each survivor is forked once, so beams share ever deeper prefixes.  Returns a list of
+    ("add", id) / ("append", id, n) / ("fork", parent, child) / ("free", id) / ("round_end", live_ids)."""
+    rng = np.random.Generator(np.random.PCG64([seed, 0]))
+    ops = [("add", 0), ("append", 0, prompt_len)]
+    live, nxt = [0], 1
+    for j in range(1, beams):
+        ops.append(("fork", 0, nxt))
+        live.append(nxt)
+        nxt += 1
+    for _ in range(rounds):
+        for b in live:
+            ops.append(("append", b, int(rng.integers(tokens_per_round[0], tokens_per_round[1], endpoint=True))))
+        keep = sorted(rng.choice(live, size=max(1, len(live) // 2), replace=False).tolist())
+        for b in live:
+            if b not in keep:
+                ops.append(("free", b))
+        live = list(keep)
+        for b in keep:
+            if len(live) < beams:
+                ops.append(("fork", b, nxt))
+                live.append(nxt)
+                nxt += 1
+        ops.append(("round_end", tuple(live)))
+    return ops
