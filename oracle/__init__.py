@@ -71,12 +71,14 @@ def lib():
             L.oracle_paged_decode.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, dbl, i32, P, i32, i32]
             L.oracle_contiguous_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, dbl, i32, P, i32,
                                                    i32]
+            L.oracle_paged_prefill.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, dbl, i32, P, i32,
+                                               i32]
             L.oracle_paged_decode_online_row.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, dbl, i32]
             L.oracle_paged_partials_row.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, dbl, i32, i32, i32]
             L.oracle_partition_merge.argtypes = [P, P, P, P, P, i32, i32, i32]
             L.oracle_num_threads.argtypes = []
             for name in ("oracle_reshape_and_cache", "oracle_copy_blocks", "oracle_swap_blocks", "oracle_paged_decode",
-                         "oracle_contiguous_decode", "oracle_paged_decode_online_row", "oracle_paged_partials_row",
+                         "oracle_contiguous_decode", "oracle_paged_prefill", "oracle_paged_decode_online_row", "oracle_paged_partials_row",
                          "oracle_partition_merge", "oracle_num_threads"):
                 getattr(L, name).restype = i32
             del i64
@@ -213,6 +215,27 @@ def contiguous_decode(q, kbuf, vbuf, req_ids, ctx, dtype, scale=None, pairs=None
                                           H_kv, D, S_max, N_max, float(scale), _dt(dtype),
                                           _ptr(pr) if pr is not None else None, npr, int(nthreads)),
            "contiguous_decode")
+    return out
+
+
+def paged_prefill(q, pool, tables, ctx, q_start, dtype, scale=None, rows=None, nthreads=1):
+    """Causal paged prefill attention, fp64.  q: [T, H_q, D] bits (rows q_start[s]..q_start[s+1]-1 are the
+    last tokens of sequence s); returns [T, H_q, D] (only ``rows`` -- flat t*H_q+h indices -- if given)."""
+    q = _c(q, np.uint16)
+    tables = _c(tables, np.int32)
+    ctx = _c(ctx, np.int32)
+    q_start = _c(q_start, np.int32)
+    T, H_q, D = q.shape
+    NB, B, _, H_kv, D2 = pool.shape
+    assert D2 == D and q_start.shape[0] == ctx.shape[0] + 1 and q_start[-1] == T
+    if scale is None:
+        scale = 1.0 / np.sqrt(float(D))
+    out = np.full((T, H_q, D), np.nan)
+    rr = None if rows is None else _c(rows, np.int32)
+    _check(lib().oracle_paged_prefill(_ptr(out), _ptr(q), _ptr(pool), _ptr(tables), _ptr(ctx), _ptr(q_start),
+                                      ctx.shape[0], H_q, H_kv, D, B, tables.shape[1], NB, float(scale), _dt(dtype),
+                                      _ptr(rr) if rr is not None else None, 0 if rr is None else rr.shape[0],
+                                      int(nthreads)), "paged_prefill")
     return out
 
 

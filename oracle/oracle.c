@@ -311,6 +311,79 @@ int oracle_contiguous_decode(double* out, const uint16_t* q, const uint16_t* kbu
 }
 
 /* ---------------------------------------------------------------------------
+ * Paged prefill attention ([PA] 実装のポイント: the paged kernel serves both the
+ * prefill and the decode phase).  Sequence s holds ctx[s] tokens in the pool;
+ * its last q_len_s = q_start[s+1] - q_start[s] tokens are the chunk being
+ * prefilled, with queries in rows q_start[s] .. q_start[s+1]-1 of q
+ * ([T][H_q][D]).  Query i of the chunk sits at position p = ctx - q_len + i and
+ * attends causally to positions 0 .. p (the decode equation with the context
+ * cut at p).  out: [T][H_q][D].  Two-pass fp64 per row, like the decode oracle.
+ * ------------------------------------------------------------------------- */
+int oracle_paged_prefill(double* out, const uint16_t* q, const uint16_t* pool, const int32_t* tables,
+                         const int32_t* ctx, const int32_t* q_start, int N, int H_q, int H_kv, int D, int B, int MB,
+                         int NB, double scale, int dtype, const int32_t* rows, int nrows, int nthreads) {
+    if (N <= 0 || H_q <= 0 || H_kv <= 0 || D <= 0 || H_q % H_kv || B <= 0 || MB <= 0 || NB <= 0) return ORC_INVALID;
+    for (int s = 0; s < N; ++s) {
+        const int ql = q_start[s + 1] - q_start[s];
+        if (ql < 0 || ql > ctx[s] || ctx[s] > MB * B || (ql == 0 && ctx[s] < 0)) return ORC_INVALID;
+    }
+    const int T = q_start[N];
+    const int G = H_q / H_kv;
+    kv_source src;
+    memset(&src, 0, sizeof src);
+    src.pool = pool;
+    src.tables = tables;
+    src.MB = MB;
+    src.NB = NB;
+    src.B = B;
+    src.H_kv = H_kv;
+    src.D = D;
+    src.paged = 1;
+    const int64_t total = rows ? nrows : (int64_t)T * H_q;
+    int status = ORC_OK;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        double* x = (double*)malloc(sizeof(double) * ((size_t)MB * B + D));
+        if (!x) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            status = ORC_NOMEM;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+            for (int64_t r = 0; r < total; ++r) {
+                /* row = (query token t, head h) */
+                const int64_t row = rows ? rows[r] : r;
+                const int t = (int)(row / H_q), h = (int)(row % H_q);
+                int s = 0;
+                while (s < N && q_start[s + 1] <= t) ++s;
+                int rc = ORC_INVALID;
+                if (t >= 0 && t < T && s < N) {
+                    const int ql = q_start[s + 1] - q_start[s];
+                    const int pos = ctx[s] - ql + (t - q_start[s]);
+                    rc = attend_one(out + row * D, q + row * D, &src, s, h, pos + 1, G, scale, dtype, x,
+                                    x + (size_t)MB * B);
+                }
+                if (rc != ORC_OK) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+                    status = rc;
+                }
+            }
+            free(x);
+        }
+    }
+    (void)nthreads;
+    return status;
+}
+
+/* ---------------------------------------------------------------------------
  * Block-streaming decode, following the explainer's paged_attention_decode
  * pseudocode ([PA] アルゴリズムの擬似コード): walk the block table in logical
  * order; for each block compute the block's scores, raise the running maximum,

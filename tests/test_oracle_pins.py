@@ -362,3 +362,53 @@ def test_swap_blocks_matches_numpy_copy_between_pools():
     for bad in ([[0, 7]], [[12, 0]], [[1, 2], [3, 2]]):
         with pytest.raises(oracle.OracleError):
             oracle.swap_blocks(host, dev, np.array(bad, dtype=np.int64))
+
+
+# ----------------------------------------------------------------------------- prefill
+
+def _prefill_case(rng, chunks, ctx, H_q=4, H_kv=2, D=16, B=4, NB=80, dtype="bf16"):
+    q_dummy, pool, tables, ctx = _tiny_paged(rng, N=len(ctx), H_q=H_q, H_kv=H_kv, D=D, B=B, NB=NB, dtype=dtype,
+                                             ctx=ctx)
+    q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    q = W.normal_bits(rng, (int(q_start[-1]), H_q, D), dtype)
+    return q, pool, tables, ctx, q_start
+
+
+def test_prefill_matches_library_causal_attention():
+    """Full prefill (chunk = whole sequence) equals torch SDPA with a causal mask in fp64; a chunk equals the
+    last rows of the full causal attention."""
+    rng = np.random.default_rng(40)
+    ctx = (9, 17, 6)
+    chunks = (9, 5, 1)
+    q, pool, tables, ctx, q_start = _prefill_case(rng, chunks, ctx)
+    got = oracle.paged_prefill(q, pool, tables, ctx, q_start, "bf16", nthreads=2)
+    kb, vb = _gather_contiguous(pool, tables, ctx)
+    for s, n in enumerate(ctx):
+        ql = int(q_start[s + 1] - q_start[s])
+        G = 2
+        k = torch.from_numpy(W.bits_to_float(kb[s, :n], "bf16").astype(np.float64)).permute(1, 0, 2)
+        v = torch.from_numpy(W.bits_to_float(vb[s, :n], "bf16").astype(np.float64)).permute(1, 0, 2)
+        k, v = k.repeat_interleave(G, 0), v.repeat_interleave(G, 0)
+        qq = torch.from_numpy(W.bits_to_float(q[q_start[s]:q_start[s + 1]], "bf16").astype(np.float64))
+        # queries sit at the last ql positions: build the [H, ql, n] causal mask explicitly
+        pos = np.arange(n - ql, n)[:, None]
+        mask = torch.from_numpy(np.arange(n)[None, :] <= pos)
+        ref = torch.nn.functional.scaled_dot_product_attention(qq.permute(1, 0, 2), k, v, attn_mask=mask)
+        np.testing.assert_allclose(got[q_start[s]:q_start[s + 1]], ref.permute(1, 0, 2).numpy(), rtol=0,
+                                   atol=1e-12)
+
+
+def test_prefill_of_one_token_is_decode():
+    rng = np.random.default_rng(41)
+    q, pool, tables, ctx, q_start = _prefill_case(rng, (1, 1, 1), (7, 13, 4))
+    pre = oracle.paged_prefill(q, pool, tables, ctx, q_start, "bf16")
+    dec = oracle.paged_decode(q, pool, tables, ctx, "bf16")
+    assert np.array_equal(pre, dec)
+
+
+def test_prefill_first_position_returns_its_own_value():
+    rng = np.random.default_rng(42)
+    q, pool, tables, ctx, q_start = _prefill_case(rng, (5,), (5,), H_q=2, H_kv=1)
+    got = oracle.paged_prefill(q, pool, tables, ctx, q_start, "bf16")
+    v0 = W.bits_to_float(pool[tables[0, 0], 0, 1, 0], "bf16").astype(np.float64)
+    assert np.array_equal(got[0, 0], v0) and np.array_equal(got[0, 1], v0)
