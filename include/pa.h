@@ -178,6 +178,25 @@ pa_status pa_decode_contiguous(void* out, pa_dtype out_dtype, const void* q, con
                                void* stream);
 
 /* ------------------------------------------------------------------------
+ * Causal paged prefill attention ([PA] 実装のポイント: the paged kernel serves
+ * the prefill phase as well as decode).  Sequence s holds ctx_lens[s] tokens
+ * in the pool, the last q_len_s = q_start[s+1] - q_start[s] of them being the
+ * chunk whose queries are rows q_start[s] .. q_start[s+1]-1 of q.  Query i of
+ * the chunk sits at position p = ctx - q_len + i and attends causally:
+ *     out[row][h] = sum_{t <= p} softmax_t(scale * q[row][h] . K_t) V_t.
+ * The chunk's own K/V must already be in the pool (pa_reshape_and_cache).
+ * q, out: [T][H_q][D] (out fp32 or the kv dtype); q_start: [N+1] int32 with
+ * q_start[0] = 0 and q_start[N] = T; max_q_len >= every chunk length.
+ * Runs on the tensor cores (tcgen05, accumulators in TMEM).  A chunk longer
+ * than its context is flagged PA_DEV_ERR_CTX and not computed.
+ * Supported: kv_dtype F16/BF16, D in {64, 128}, B in {8, 16, 32},
+ * H_q / H_kv <= 128, N <= 65535.
+ * ---------------------------------------------------------------------- */
+pa_status pa_prefill(void* out, pa_dtype out_dtype, const void* q, const void* pool, const int32_t* block_tables,
+                     const int32_t* ctx_lens, const int32_t* q_start, int N, int T, int H_q, int H_kv, int D, int B,
+                     int MB, int NB, int max_q_len, float scale, pa_dtype kv_dtype, int* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
  * pa_decode without a caller-provided workspace.  The pages have no
  * counterpart: this entry point exists for callers that cannot allocate device
  * memory where they decode (a plug-in inside a framework that owns every

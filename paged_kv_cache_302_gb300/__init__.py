@@ -83,6 +83,7 @@ def _declare(L):
         "pa_alloc_append_batch": ([P, i32, P, P, P, P, i32, P, P, i32, P], i32),
         "pa_update_block_tables": ([P, i32, i32, P, i32, P, P], i32),
         "pa_swap_blocks": ([P, i32, P, i32, P, i32, i32, i32, i32, i32, P, P], i32),
+        "pa_prefill": ([P, i32, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, P, P], i32),
         "pa_alloc_fork": ([P, i32, i32], i32),
         "pa_alloc_free_seq": ([P, i32], i32),
         "pa_alloc_block_table": ([P, i32, P, i32, P], i32),
@@ -317,6 +318,24 @@ def pa_decode_contiguous(out, q, k_buf, v_buf, req_ids, ctx_lens, max_ctx, scale
                                   int(max_ctx), scale, int(partition_tokens), _dev(ws, "workspace"),
                                   ws.numel() * ws.element_size(), _dtype_code(k_buf.dtype), _err_ptr(dev_err),
                                   _events_arg(attend_events, stream), _stream_ptr(stream)))
+    return out
+
+
+def pa_prefill(out, q, pool, block_tables, ctx_lens, q_start, max_q_len, scale=None, dev_err=None, stream=None):
+    """Causal paged prefill: q, out [T, H_q, D]; q_start [N+1] int32 (device); chunks are the sequences' last
+    tokens, already written to the pool."""
+    T, H_q, D = q.shape
+    NB, B, _, H_kv, D2 = pool.shape
+    N = ctx_lens.numel()
+    MB = block_tables.shape[1]
+    if D2 != D or tuple(out.shape) != (T, H_q, D) or q.dtype != pool.dtype or q_start.numel() != N + 1:
+        raise PAError(PA_ERR_INVALID, "shape/dtype mismatch")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    L = load()
+    _check(L.pa_prefill(_dev(out, "out"), _dtype_code(out.dtype), _dev(q, "q"), _dev(pool, "pool"),
+                        _dev(block_tables, "block_tables", torch.int32), _dev(ctx_lens, "ctx_lens", torch.int32),
+                        _dev(q_start, "q_start", torch.int32), N, T, H_q, H_kv, D, B, MB, NB, int(max_q_len), scale,
+                        _dtype_code(pool.dtype), _err_ptr(dev_err), _stream_ptr(stream)))
     return out
 
 

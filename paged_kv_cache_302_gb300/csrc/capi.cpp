@@ -229,6 +229,48 @@ pa_status pa_decode_contiguous(void* out, pa_dtype out_dtype, const void* q, con
     return launch_decode(a);
 }
 
+pa_status pa_prefill(void* out, pa_dtype out_dtype, const void* q, const void* pool, const int32_t* block_tables,
+                     const int32_t* ctx_lens, const int32_t* q_start, int N, int T, int H_q, int H_kv, int D, int B,
+                     int MB, int NB, int max_q_len, float scale, pa_dtype kv_dtype, int* dev_err, void* stream) {
+    g_msg[0] = 0;
+    if (!kv_dtype_ok(kv_dtype)) return fail(PA_ERR_UNSUPPORTED, "kv_dtype must be F16 or BF16");
+    if (out_dtype != PA_F32 && out_dtype != kv_dtype)
+        return fail(PA_ERR_UNSUPPORTED, "out_dtype must be F32 or the kv dtype");
+    if (N <= 0 || N > 65535 || T < 0 || H_q <= 0 || H_kv <= 0 || H_kv > 65535 || MB <= 0 || NB <= 0 ||
+        max_q_len < 0)
+        return fail(PA_ERR_INVALID, "bad sizes");
+    if (H_q % H_kv) return fail(PA_ERR_INVALID, "H_q must be a multiple of H_kv");
+    if (H_q / H_kv > 128) return fail(PA_ERR_UNSUPPORTED, "H_q / H_kv must be <= 128");
+    if (D != 64 && D != 128) return fail(PA_ERR_UNSUPPORTED, "D must be 64 or 128");
+    if (B != 8 && B != 16 && B != 32) return fail(PA_ERR_UNSUPPORTED, "prefill supports B in {8, 16, 32}");
+    if ((long long)NB * B >= (1LL << 31)) return fail(PA_ERR_UNSUPPORTED, "NB * B must be < 2^31");
+    if (T == 0 || max_q_len == 0) return PA_OK;
+    if (!out || !q || !pool || !block_tables || !ctx_lens || !q_start) return fail(PA_ERR_INVALID, "null pointer");
+    if (!aligned16(out) || !aligned16(q) || !aligned16(pool)) return fail(PA_ERR_INVALID, "16-byte alignment");
+    PrefillArgs a;
+    a.out = out;
+    a.out_dtype = out_dtype;
+    a.q = q;
+    a.pool = pool;
+    a.tables = block_tables;
+    a.ctx_lens = ctx_lens;
+    a.q_start = q_start;
+    a.N = N;
+    a.T = T;
+    a.H_q = H_q;
+    a.H_kv = H_kv;
+    a.D = D;
+    a.B = B;
+    a.MB = MB;
+    a.NB = NB;
+    a.max_q_len = max_q_len;
+    a.scale = scale;
+    a.kv_dtype = kv_dtype;
+    a.dev_err = dev_err;
+    a.stream = static_cast<cudaStream_t>(stream);
+    return launch_prefill(a);
+}
+
 pa_status pa_partition_reduce(void* out, pa_dtype out_dtype, const float* part_m2, const float* part_l,
                               const float* part_acc, const int32_t* nparts, int R, int P, int D, int* dev_err,
                               void* stream) {

@@ -76,6 +76,23 @@ struct DecodeArgs {
 
 pa_status launch_decode(const DecodeArgs& a);
 
+struct PrefillArgs {
+    void* out;
+    int out_dtype;
+    const void* q;
+    const void* pool;
+    const int32_t* tables;
+    const int32_t* ctx_lens;
+    const int32_t* q_start;
+    int N, T, H_q, H_kv, D, B, MB, NB, max_q_len;
+    float scale;
+    int kv_dtype;
+    int* dev_err;
+    cudaStream_t stream;
+};
+
+pa_status launch_prefill(const PrefillArgs& a);
+
 pa_status launch_partition_reduce(void* out, int out_dtype, const float* m2, const float* l, const float* acc,
                                   const int32_t* nparts, int rows_per_seq, int R, int P, int D, bool skip_single,
                                   int* dev_err, cudaStream_t stream);

@@ -1,0 +1,459 @@
+// prefill.cu -- causal paged prefill attention on the sm_103a tensor cores (tcgen05 + TMEM).
+//
+// Method: PagedAttention explainer (0h-n0.github.io, arXiv 2309.06180), 実装のポイント:
+// the paged kernel serves the prefill phase as well as decode -- a chunk of a
+// sequence's newest tokens attends, causally, to the whole context through
+// the block table.  Each query row follows the decode equation with its
+// context cut at its own position.
+//
+// One CTA (4 warps) owns a tile of 128 query rows: 128/G query tokens times the
+// G query heads of one KV head, so every K/V byte a tile loads serves G heads.
+// Per 128-key tile:
+//   * TMA lands the tile's K and V rows (one box per KV block and 64-column
+//     half, 128-byte swizzled) through the block table;
+//   * one thread issues S = Q K^T as tcgen05.mma (M 128, N 128, K 16 steps)
+//     into TMEM columns [0, 128);
+//   * every thread owns one TMEM lane = one query row: it reads its S row with
+//     tcgen05.ld, masks causally, keeps the running maximum (rescaling the
+//     output only when the maximum grows by more than 2^8), and writes the
+//     probabilities to shared memory as a high and a low 16-bit part;
+//   * one thread issues O += P_hi V + P_lo V (V is an MN-major operand) into
+//     TMEM columns [128, 128 + D).
+// Finally every thread reads its O row, divides by its exponential sum and
+// stores the row.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <type_traits>
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+constexpr int kPfRows = 128;     // query rows per CTA (tcgen05 M)
+constexpr int kPfKeys = 128;     // keys per tile (tcgen05 N of S, K of P V)
+constexpr int kPfThreads = 128;  // one thread per row / TMEM lane
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kRegion = kPfRows * 128;  // one [128 rows][64 columns] 16-bit swizzled region: 16 KB
+
+struct PrefillParams {
+    const int32_t* tables;
+    const int32_t* ctx_lens;
+    const int32_t* q_start;
+    int N, T, H_q, H_kv, G, TQ, B, MB, NB;
+    void* out;
+    int out_dtype;
+    float scale_log2;
+    int* err;
+};
+
+// ----------------------------------------------------------------------------- tcgen05 wrappers
+
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 encoding: address, leading and stride byte
+// offsets in 16-byte units, descriptor version 1 at bit 46, layout code 2 at bit 61).
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with an fp32 accumulator.
+__host__ __device__ constexpr uint32_t umma_idesc(bool bf16, int M, int N, bool b_mn_major) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t mbar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ----------------------------------------------------------------------------- kernel
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                                const __grid_constant__ CUtensorMap tm_kv,
+                                                                const PrefillParams p) {
+    constexpr int DH = D / 64;          // 64-column halves of a head row
+    constexpr int NK = D / 16;          // k-steps of S = Q K^T
+    constexpr int NT = kPfKeys / 16;    // k-steps of O += P V
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t idesc_s = umma_idesc(kBf16, kPfRows, kPfKeys, false);
+    constexpr uint32_t idesc_o = umma_idesc(kBf16, kPfRows, D, true);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_addr(base);
+    const uint32_t sQ = sb, sK = sQ + DH * kRegion, sV = sK + DH * kRegion, sPh = sV + DH * kRegion,
+                   sPl = sPh + 2 * kRegion, sBar = sPl + 2 * kRegion;
+    const uint32_t qbar = sBar, kvbar = sBar + 8, sbar = sBar + 16, pvbar = sBar + 24;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + (sBar - sb) + 32);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + (sBar - sb) + 36);
+
+    griddep_wait();
+    griddep_launch_dependents();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int s = blockIdx.z, g = blockIdx.y;
+    const int qs = p.q_start[s], q_len = p.q_start[s + 1] - qs;
+    const int tok0 = blockIdx.x * p.TQ;
+    if (tok0 >= q_len) return;  // uniform per CTA, before any allocation
+    const int ctx = p.ctx_lens[s];
+    if (q_len > ctx || ctx > p.MB * p.B || q_len < 0) {
+        if (tid == 0) flag_error(p.err, PA_DEV_ERR_CTX);
+        return;
+    }
+    const int pos0 = ctx - q_len + tok0;                         // position of the tile's first query token
+    const int last_tok = min(tok0 + p.TQ, q_len) - 1;
+    const int nkeys = ctx - q_len + last_tok + 1;                // keys the tile's last query sees
+    const int ntiles = (nkeys + kPfKeys - 1) / kPfKeys;
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid == 0) {
+        mbar_init(qbar, 1);
+        mbar_init(kvbar, 1);
+        mbar_init(sbar, 1);
+        mbar_init(pvbar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    // rows past TQ*G (when G does not divide 128) are never loaded: clear them once
+    for (int r = p.TQ * p.G + warp; r < kPfRows; r += 4)
+        for (int dh = 0; dh < DH; ++dh)
+            if (lane < 8)
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sQ + dh * kRegion + r * 128 + lane * 16),
+                             "r"(0)
+                             : "memory");
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's 32 lanes
+    const uint64_t pol = policy_evict_first();
+
+    // producer (thread 0): the K and V rows of key tile j
+    auto issue_tile = [&](int j) {
+        const int k0 = j * kPfKeys;
+        const int lb0 = k0 / p.B;
+        const int nb = min(kPfKeys, ctx - k0 + p.B - 1) / p.B;  // blocks holding keys of this tile
+        const int nblk = min(nb, kPfKeys / p.B);
+        mbar_arrive_expect_tx(kvbar, (uint32_t)nblk * DH * 2 * p.B * 128);
+        for (int b = 0; b < nblk; ++b) {
+            int e = p.tables[(size_t)s * p.MB + lb0 + b];
+            if ((unsigned)e >= (unsigned)p.NB) {
+                flag_error(p.err, PA_DEV_ERR_BLOCK);
+                e = p.NB;
+            }
+            for (int dh = 0; dh < DH; ++dh) {
+                const uint32_t off = dh * kRegion + (uint32_t)b * p.B * 128;
+                tma_load_5d(sK + off, &tm_kv, kvbar, 0, e * p.B, dh, g, 0, pol);
+                tma_load_5d(sV + off, &tm_kv, kvbar, 0, e * p.B, dh, g, 1, pol);
+            }
+        }
+    };
+    if (tid == 0) {
+        mbar_arrive_expect_tx(qbar, (uint32_t)DH * p.G * p.TQ * 128);
+        for (int dh = 0; dh < DH; ++dh)
+            tma_load_4d(sQ + dh * kRegion, &tm_q, qbar, 0, dh, g * p.G, qs + tok0, policy_evict_normal());
+        issue_tile(0);
+    }
+
+    // this thread's query row
+    const int r = tid;
+    const int qtok = r / p.G;
+    const bool row_ok = r < p.TQ * p.G && tok0 + qtok < q_len;
+    const int qpos = row_ok ? pos0 + qtok : -1;  // -1 masks every key
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = mbar_wait_bounded(qbar, 0, abort_flag);
+    const float NEG_INF = -INFINITY;
+
+    // A wait that runs out sets the abort flag (later waits then return at once); every thread still
+    // passes the same barriers and the loop ends together after the tile.
+    auto waited = [&](uint32_t bar, uint32_t parity) {
+        const bool w = mbar_wait_bounded(bar, parity, abort_flag);
+        if (!w) *abort_flag = 1;
+        return w;
+    };
+    if (!ok) *abort_flag = 1;
+    ok = __syncthreads_and(ok);
+    for (int j = 0; j < ntiles && ok; ++j) {
+        const uint32_t ph = (uint32_t)(j & 1);
+        ok = waited(kvbar, ph);
+        const int k0 = j * kPfKeys;
+        // V rows past the context may hold anything (even NaN): zero them before they meet P = 0
+        const int nvalid = min(kPfKeys, ctx - k0);
+        if (nvalid < kPfKeys) {
+            for (int rr = nvalid + warp; rr < kPfKeys; rr += 4)
+                for (int dh = 0; dh < DH; ++dh)
+                    if (lane < 8)
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sV + dh * kRegion + rr * 128 +
+                                                                                      lane * 16),
+                                     "r"(0)
+                                     : "memory");
+            fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < NK; ++ks) {
+                const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
+                umma_f16(tmem, umma_desc(sQ + off, 16, 1024), umma_desc(sK + off, 16, 1024), idesc_s, ks > 0);
+            }
+            umma_commit(sbar);
+        }
+        ok = waited(sbar, ph) && ok;
+        tc_fence_after();
+
+        // ---- online softmax on this thread's row (base 2)
+        float m_tile = NEG_INF;
+#pragma unroll
+        for (int c = 0; c < kPfKeys / 32; ++c) {
+            float v[32];
+            tmem_ld32(t_lane + c * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (k0 + c * 32 + i <= qpos) m_tile = fmaxf(m_tile, v[i] * p.scale_log2);
+        }
+        float m_new = m_ref;
+        if (j == 0 || m_tile > m_ref + 8.f) m_new = fmaxf(m_ref, m_tile);
+        const float m_use = m_new == NEG_INF ? 0.f : m_new;
+        const float alpha = (j == 0 || m_new == m_ref) ? 1.f : fast_exp2(m_ref - m_new);
+        l *= alpha;
+        m_ref = m_new;
+#pragma unroll
+        for (int c = 0; c < kPfKeys / 32; ++c) {
+            float v[32];
+            tmem_ld32(t_lane + c * 32, v);
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const float p0 = k0 + c * 32 + i <= qpos ? fast_exp2(v[i] * p.scale_log2 - m_use) : 0.f;
+                const float p1 = k0 + c * 32 + i + 1 <= qpos ? fast_exp2(v[i + 1] * p.scale_log2 - m_use) : 0.f;
+                l += p0 + p1;
+                hi[i / 2] = Mma<T>::pack(p0, p1);
+                const float2 f = Mma<T>::unpack(hi[i / 2]);
+                lo[i / 2] = Mma<T>::pack(p0 - f.x, p1 - f.y);
+            }
+            // keys c*32 .. c*32+31 = 16-byte units u of the 64-key half c/2
+            const uint32_t row_off = (uint32_t)(c >> 1) * kRegion + (uint32_t)r * 128;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t unit = (uint32_t)((c & 1) * 4 + u) ^ (uint32_t)(r & 7);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sPh + row_off + unit * 16),
+                             "r"(hi[4 * u]), "r"(hi[4 * u + 1]), "r"(hi[4 * u + 2]), "r"(hi[4 * u + 3])
+                             : "memory");
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sPl + row_off + unit * 16),
+                             "r"(lo[4 * u]), "r"(lo[4 * u + 1]), "r"(lo[4 * u + 2]), "r"(lo[4 * u + 3])
+                             : "memory");
+            }
+        }
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                float v[32];
+                tmem_ld32(t_lane + kPfKeys + c * 32, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] *= alpha;
+                tmem_st32(t_lane + kPfKeys + c * 32, v);
+            }
+            tmem_wait_st();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < NT; ++ks) {
+                const uint32_t aoff = (ks >> 2) * kRegion + (ks & 3) * 32;
+                const uint64_t vdesc = umma_desc(sV + ks * 16 * 128, kRegion, 1024);
+                umma_f16(tmem + kPfKeys, umma_desc(sPh + aoff, 16, 1024), vdesc, idesc_o, (j > 0 || ks > 0));
+                umma_f16(tmem + kPfKeys, umma_desc(sPl + aoff, 16, 1024), vdesc, idesc_o, 1u);
+            }
+            umma_commit(pvbar);
+            // the next tile's K and V overwrite this tile's once the products are done
+            ok = waited(pvbar, ph) && ok;
+            if (ok && j + 1 < ntiles) issue_tile(j + 1);
+        }
+        ok = __syncthreads_and(ok);
+    }
+    if (ok) ok = waited(pvbar, (uint32_t)((ntiles - 1) & 1));
+    else mbar_wait_bounded(pvbar, (uint32_t)((ntiles - 1) & 1), nullptr, 1000000ull);  // let issued work land
+    if (!ok) {
+        if (tid == 0) {
+            flag_error(p.err, PA_DEV_ERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+    } else {
+        tc_fence_after();
+        const float inv = 1.f / l;
+        const size_t orow = ((size_t)(qs + tok0 + qtok) * p.H_q + (size_t)g * p.G + (r % p.G)) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            float v[32];
+            tmem_ld32(t_lane + kPfKeys + c * 32, v);
+            if (row_ok) {
+                if (p.out_dtype == PA_F32) {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+                } else {
+                    T* dst = static_cast<T*>(p.out) + orow + c * 32;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) dst[i] = from_float<T>(v[i] * inv);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+// ----------------------------------------------------------------------------- host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn pf_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+static size_t prefill_smem_bytes(int D) {
+    const int DH = D / 64;
+    return 1024 + (size_t)(3 * DH + 4) * kRegion + 64;
+}
+
+template <typename T, int D>
+static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tkv) {
+    auto kern = prefill_kernel<T, D>;
+    const size_t smem = prefill_smem_bytes(D);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill)");
+    PrefillParams p;
+    p.tables = a.tables;
+    p.ctx_lens = a.ctx_lens;
+    p.q_start = a.q_start;
+    p.N = a.N;
+    p.T = a.T;
+    p.H_q = a.H_q;
+    p.H_kv = a.H_kv;
+    p.G = a.H_q / a.H_kv;
+    p.TQ = kPfRows / p.G;
+    p.B = a.B;
+    p.MB = a.MB;
+    p.NB = a.NB;
+    p.out = a.out;
+    p.out_dtype = a.out_dtype;
+    p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
+    p.err = a.dev_err;
+    const dim3 grid((a.max_q_len + p.TQ - 1) / p.TQ, a.H_kv, a.N);
+    e = launch_kernel(kern, grid, dim3(kPfThreads), smem, a.stream, tq, tkv, p);
+    count_launch();
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "prefill launch");
+}
+
+pa_status launch_prefill(const PrefillArgs& a) {
+    EncodeTiledFn fn = pf_encode_fn();
+    if (!fn) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const int DH = a.D / 64, G = a.H_q / a.H_kv, TQ = kPfRows / G;
+    const CUtensorMapDataType dt =
+        a.kv_dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUtensorMap tq, tkv;
+    std::memset(&tq, 0, sizeof tq);
+    std::memset(&tkv, 0, sizeof tkv);
+    // queries [T][H_q][D]: dims 64 columns, column half, head, token; box = G heads x TQ tokens
+    cuuint64_t qd[4] = {64, (cuuint64_t)DH, (cuuint64_t)a.H_q, (cuuint64_t)a.T};
+    cuuint64_t qs[3] = {128, (cuuint64_t)a.D * 2, (cuuint64_t)a.H_q * a.D * 2};
+    cuuint32_t qb[4] = {64, 1, (cuuint32_t)G, (cuuint32_t)TQ};
+    CUresult r = fn(&tq, dt, 4, const_cast<void*>(a.q), qd, qs, qb, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(q) failed (CUresult %d)", (int)r);
+    // pool [NB][B][2][H_kv][D]: dims 64 columns, token, column half, kv head, K/V; box = one block, one half
+    cuuint64_t pd[5] = {64, (cuuint64_t)a.NB * a.B, (cuuint64_t)DH, (cuuint64_t)a.H_kv, 2};
+    cuuint64_t ps[4] = {(cuuint64_t)2 * a.H_kv * a.D * 2, 128, (cuuint64_t)a.D * 2, (cuuint64_t)a.H_kv * a.D * 2};
+    cuuint32_t pb[5] = {64, (cuuint32_t)a.B, 1, 1, 1};
+    r = fn(&tkv, dt, 5, const_cast<void*>(a.pool), pd, ps, pb, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(pool) failed (CUresult %d)", (int)r);
+    if (a.kv_dtype == PA_BF16)
+        return a.D == 128 ? run_prefill<__nv_bfloat16, 128>(a, tq, tkv) : run_prefill<__nv_bfloat16, 64>(a, tq, tkv);
+    return a.D == 128 ? run_prefill<__half, 128>(a, tq, tkv) : run_prefill<__half, 64>(a, tq, tkv);
+}
+
+}  // namespace pa
