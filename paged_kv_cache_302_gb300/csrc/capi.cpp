@@ -243,6 +243,7 @@ pa_status pa_prefill(void* out, pa_dtype out_dtype, const void* q, const void* p
     if (H_q / H_kv > 128) return fail(PA_ERR_UNSUPPORTED, "H_q / H_kv must be <= 128");
     if (D != 64 && D != 128) return fail(PA_ERR_UNSUPPORTED, "D must be 64 or 128");
     if (B != 8 && B != 16 && B != 32) return fail(PA_ERR_UNSUPPORTED, "prefill supports B in {8, 16, 32}");
+    if (!(scale > 0.f)) return fail(PA_ERR_INVALID, "scale must be positive");
     if ((long long)NB * B >= (1LL << 31)) return fail(PA_ERR_UNSUPPORTED, "NB * B must be < 2^31");
     if (T == 0 || max_q_len == 0) return PA_OK;
     if (!out || !q || !pool || !block_tables || !ctx_lens || !q_start) return fail(PA_ERR_INVALID, "null pointer");

@@ -34,8 +34,8 @@ namespace pa {
 
 constexpr int kPfRows = 128;     // query rows per CTA (tcgen05 M)
 constexpr int kPfKeys = 128;     // keys per tile (tcgen05 N of S, K of P V)
-constexpr int kPfThreads = 128;  // one thread per row / TMEM lane
-constexpr uint32_t kTmemCols = 256;
+constexpr int kPfThreads = 192;  // warps 0-3: one thread per row / TMEM lane; 4: TMA; 5: MMA
+constexpr uint32_t kTmemCols = 512;  // S[0], S[1] (128 columns each), O (D columns)
 constexpr uint32_t kRegion = kPfRows * 128;  // one [128 rows][64 columns] 16-bit swizzled region: 16 KB
 
 struct PrefillParams {
@@ -133,14 +133,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t idesc_s = umma_idesc(kBf16, kPfRows, kPfKeys, false);
     constexpr uint32_t idesc_o = umma_idesc(kBf16, kPfRows, D, true);
+    constexpr uint32_t kTile = DH * kRegion;  // one K (or V) tile: 128 keys x D
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_addr(base);
-    const uint32_t sQ = sb, sK = sQ + DH * kRegion, sV = sK + DH * kRegion, sPh = sV + DH * kRegion,
-                   sPl = sPh + 2 * kRegion, sBar = sPl + 2 * kRegion;
-    const uint32_t qbar = sBar, kvbar = sBar + 8, sbar = sBar + 16, pvbar = sBar + 24;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + (sBar - sb) + 32);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + (sBar - sb) + 36);
+    // Q | K[2] | V[2] | P_hi | P_lo | barriers
+    const uint32_t sQ = sb, sK0 = sQ + kTile, sV0 = sK0 + 2 * kTile, sPh = sV0 + 2 * kTile, sPl = sPh + 2 * kRegion,
+                   sBar = sPl + 2 * kRegion;
+    // barriers: q, k[2], v[2], s[2], pv[2], p_ready
+    const uint32_t qbar = sBar, kbar0 = sBar + 8, vbar0 = sBar + 24, sbar0 = sBar + 40, pvbar0 = sBar + 56,
+                   pready = sBar + 72;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + (sBar - sb) + 80);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + (sBar - sb) + 84);
 
     griddep_wait();
     griddep_launch_dependents();
@@ -166,207 +170,252 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        mbar_init(qbar, 1);
-        mbar_init(kvbar, 1);
-        mbar_init(sbar, 1);
-        mbar_init(pvbar, 1);
+        for (int i = 0; i < 9; ++i) mbar_init(sBar + 8 * i, 1);
+        mbar_init(pready, kPfRows);
         *abort_flag = 0;
         fence_mbar_init();
     }
     // rows past TQ*G (when G does not divide 128) are never loaded: clear them once
-    for (int r = p.TQ * p.G + warp; r < kPfRows; r += 4)
-        for (int dh = 0; dh < DH; ++dh)
-            if (lane < 8)
-                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sQ + dh * kRegion + r * 128 + lane * 16),
-                             "r"(0)
-                             : "memory");
+    if (warp < 4)
+        for (int r = p.TQ * p.G + warp; r < kPfRows; r += 4)
+            for (int dh = 0; dh < DH; ++dh)
+                if (lane < 8)
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sQ + dh * kRegion + r * 128 +
+                                                                                  lane * 16),
+                                 "r"(0)
+                                 : "memory");
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's 32 lanes
-    const uint64_t pol = policy_evict_first();
-
-    // producer (thread 0): the K and V rows of key tile j
-    auto issue_tile = [&](int j) {
-        const int k0 = j * kPfKeys;
-        const int lb0 = k0 / p.B;
-        const int nb = min(kPfKeys, ctx - k0 + p.B - 1) / p.B;  // blocks holding keys of this tile
-        const int nblk = min(nb, kPfKeys / p.B);
-        mbar_arrive_expect_tx(kvbar, (uint32_t)nblk * DH * 2 * p.B * 128);
-        for (int b = 0; b < nblk; ++b) {
-            int e = p.tables[(size_t)s * p.MB + lb0 + b];
-            if ((unsigned)e >= (unsigned)p.NB) {
-                flag_error(p.err, PA_DEV_ERR_BLOCK);
-                e = p.NB;
-            }
-            for (int dh = 0; dh < DH; ++dh) {
-                const uint32_t off = dh * kRegion + (uint32_t)b * p.B * 128;
-                tma_load_5d(sK + off, &tm_kv, kvbar, 0, e * p.B, dh, g, 0, pol);
-                tma_load_5d(sV + off, &tm_kv, kvbar, 0, e * p.B, dh, g, 1, pol);
-            }
-        }
-    };
-    if (tid == 0) {
-        mbar_arrive_expect_tx(qbar, (uint32_t)DH * p.G * p.TQ * 128);
-        for (int dh = 0; dh < DH; ++dh)
-            tma_load_4d(sQ + dh * kRegion, &tm_q, qbar, 0, dh, g * p.G, qs + tok0, policy_evict_normal());
-        issue_tile(0);
-    }
-
-    // this thread's query row
-    const int r = tid;
-    const int qtok = r / p.G;
-    const bool row_ok = r < p.TQ * p.G && tok0 + qtok < q_len;
-    const int qpos = row_ok ? pos0 + qtok : -1;  // -1 masks every key
-    float m_ref = -INFINITY, l = 0.f;
-    bool ok = mbar_wait_bounded(qbar, 0, abort_flag);
-    const float NEG_INF = -INFINITY;
-
-    // A wait that runs out sets the abort flag (later waits then return at once); every thread still
-    // passes the same barriers and the loop ends together after the tile.
+    const uint32_t tmem = *tmem_slot;              // columns: S[0] 0..127, S[1] 128..255, O 256..
+    const uint32_t col_o = 2 * kPfKeys;
     auto waited = [&](uint32_t bar, uint32_t parity) {
         const bool w = mbar_wait_bounded(bar, parity, abort_flag);
         if (!w) *abort_flag = 1;
         return w;
     };
-    if (!ok) *abort_flag = 1;
-    ok = __syncthreads_and(ok);
-    for (int j = 0; j < ntiles && ok; ++j) {
-        const uint32_t ph = (uint32_t)(j & 1);
-        ok = waited(kvbar, ph);
-        const int k0 = j * kPfKeys;
-        // V rows past the context may hold anything (even NaN): zero them before they meet P = 0
-        const int nvalid = min(kPfKeys, ctx - k0);
-        if (nvalid < kPfKeys) {
-            for (int rr = nvalid + warp; rr < kPfKeys; rr += 4)
-                for (int dh = 0; dh < DH; ++dh)
-                    if (lane < 8)
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sV + dh * kRegion + rr * 128 +
-                                                                                      lane * 16),
-                                     "r"(0)
-                                     : "memory");
-            fence_proxy_async_smem();
+    bool ok = true;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ TMA producer
+        const uint64_t pol = policy_evict_first();
+        if (lane == 0) {
+            mbar_arrive_expect_tx(qbar, (uint32_t)DH * p.G * p.TQ * 128);
+            for (int dh = 0; dh < DH; ++dh)
+                tma_load_4d(sQ + dh * kRegion, &tm_q, qbar, 0, dh, g * p.G, qs + tok0, policy_evict_normal());
         }
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
+        for (int t = 0; t < ntiles && ok; ++t) {
+            const int k0 = t * kPfKeys;
+            const int nblk = min(kPfKeys, ctx - k0 + p.B - 1) / p.B;  // blocks holding keys of this tile
+            int mine = lane < nblk ? p.tables[(size_t)s * p.MB + k0 / p.B + lane] : 0;
+            if (lane < nblk && (unsigned)mine >= (unsigned)p.NB) {
+                flag_error(p.err, PA_DEV_ERR_BLOCK);
+                mine = p.NB;  // past the tensor: TMA fills zeros
+            }
+            const uint32_t bytes = (uint32_t)nblk * DH * p.B * 128;
+            const uint32_t b2 = (uint32_t)(t & 1);
+            for (int which = 0; which < 2 && ok; ++which) {
+                // buffer t % 2 is free once S_{t-2} (for K) / PV_{t-2} (for V) is done
+                if (t >= 2) ok = waited((which ? pvbar0 : sbar0) + 8 * b2, (uint32_t)(((t - 2) >> 1) & 1));
+                if (!ok) break;
+                const uint32_t bar = (which ? vbar0 : kbar0) + 8 * b2;
+                const uint32_t dst = (which ? sV0 : sK0) + b2 * kTile;
+                if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+                for (int b = 0; b < nblk; ++b) {
+                    const int e = __shfl_sync(0xffffffffu, mine, b);
+                    if (lane == 0)
+                        for (int dh = 0; dh < DH; ++dh)
+                            tma_load_5d(dst + dh * kRegion + (uint32_t)b * p.B * 128, &tm_kv, bar, 0, e * p.B, dh, g,
+                                        which, pol);
+                }
+            }
+            ok = __all_sync(0xffffffffu, ok);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        auto issue_s = [&](int j) {  // S[j % 2] = Q K_j^T
+            const uint32_t kb = sK0 + (uint32_t)(j & 1) * kTile;
 #pragma unroll
             for (int ks = 0; ks < NK; ++ks) {
                 const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
-                umma_f16(tmem, umma_desc(sQ + off, 16, 1024), umma_desc(sK + off, 16, 1024), idesc_s, ks > 0);
+                umma_f16(tmem + (uint32_t)(j & 1) * kPfKeys, umma_desc(sQ + off, 16, 1024),
+                         umma_desc(kb + off, 16, 1024), idesc_s, ks > 0);
             }
-            umma_commit(sbar);
-        }
-        ok = waited(sbar, ph) && ok;
-        tc_fence_after();
-
-        // ---- online softmax on this thread's row (base 2)
-        float m_tile = NEG_INF;
-#pragma unroll
-        for (int c = 0; c < kPfKeys / 32; ++c) {
-            float v[32];
-            tmem_ld32(t_lane + c * 32, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (k0 + c * 32 + i <= qpos) m_tile = fmaxf(m_tile, v[i] * p.scale_log2);
-        }
-        float m_new = m_ref;
-        if (j == 0 || m_tile > m_ref + 8.f) m_new = fmaxf(m_ref, m_tile);
-        const float m_use = m_new == NEG_INF ? 0.f : m_new;
-        const float alpha = (j == 0 || m_new == m_ref) ? 1.f : fast_exp2(m_ref - m_new);
-        l *= alpha;
-        m_ref = m_new;
-#pragma unroll
-        for (int c = 0; c < kPfKeys / 32; ++c) {
-            float v[32];
-            tmem_ld32(t_lane + c * 32, v);
-            uint32_t hi[16], lo[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const float p0 = k0 + c * 32 + i <= qpos ? fast_exp2(v[i] * p.scale_log2 - m_use) : 0.f;
-                const float p1 = k0 + c * 32 + i + 1 <= qpos ? fast_exp2(v[i + 1] * p.scale_log2 - m_use) : 0.f;
-                l += p0 + p1;
-                hi[i / 2] = Mma<T>::pack(p0, p1);
-                const float2 f = Mma<T>::unpack(hi[i / 2]);
-                lo[i / 2] = Mma<T>::pack(p0 - f.x, p1 - f.y);
+            umma_commit(sbar0 + 8 * (j & 1));
+        };
+        if (lane == 0) {
+            ok = waited(qbar, 0) && waited(kbar0, 0);
+            tc_fence_after();
+            if (ok) issue_s(0);
+            if (ok && ntiles > 1) {
+                ok = waited(kbar0 + 8, 0);
+                if (ok) issue_s(1);
             }
-            // keys c*32 .. c*32+31 = 16-byte units u of the 64-key half c/2
-            const uint32_t row_off = (uint32_t)(c >> 1) * kRegion + (uint32_t)r * 128;
+            for (int j = 0; j < ntiles && ok; ++j) {
+                ok = waited(pready, (uint32_t)(j & 1)) && waited(vbar0 + 8 * (j & 1), (uint32_t)((j >> 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t vb = sV0 + (uint32_t)(j & 1) * kTile;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t unit = (uint32_t)((c & 1) * 4 + u) ^ (uint32_t)(r & 7);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sPh + row_off + unit * 16),
-                             "r"(hi[4 * u]), "r"(hi[4 * u + 1]), "r"(hi[4 * u + 2]), "r"(hi[4 * u + 3])
-                             : "memory");
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sPl + row_off + unit * 16),
-                             "r"(lo[4 * u]), "r"(lo[4 * u + 1]), "r"(lo[4 * u + 2]), "r"(lo[4 * u + 3])
-                             : "memory");
+                for (int ks = 0; ks < NT; ++ks) {
+                    const uint32_t aoff = (ks >> 2) * kRegion + (ks & 3) * 32;
+                    const uint64_t vdesc = umma_desc(vb + ks * 16 * 128, kRegion, 1024);
+                    umma_f16(tmem + col_o, umma_desc(sPh + aoff, 16, 1024), vdesc, idesc_o, (j > 0 || ks > 0));
+                    umma_f16(tmem + col_o, umma_desc(sPl + aoff, 16, 1024), vdesc, idesc_o, 1u);
+                }
+                umma_commit(pvbar0 + 8 * (j & 1));
+                if (j + 2 < ntiles) {
+                    ok = waited(kbar0 + 8 * (j & 1), (uint32_t)(((j + 2) >> 1) & 1));
+                    if (ok) issue_s(j + 2);  // S[j % 2] was read by softmax j, which signalled p_ready
+                }
             }
         }
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax warps: thread = query row = TMEM lane
+        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+        const int r = tid;
+        const int qtok = r / p.G;
+        const bool row_ok = r < p.TQ * p.G && tok0 + qtok < q_len;
+        const int qpos = row_ok ? pos0 + qtok : -1;  // -1 masks every key
+        float m_ref = -INFINITY, l = 0.f;
+        const float NEG_INF = -INFINITY;
+        for (int j = 0; j < ntiles; ++j) {
+            const int k0 = j * kPfKeys;
+            ok = waited(sbar0 + 8 * (j & 1), (uint32_t)((j >> 1) & 1)) && ok;
+            tc_fence_after();
+            const uint32_t t_s = t_lane + (uint32_t)(j & 1) * kPfKeys;
+            float v[kPfKeys];
+            {
+                uint32_t* u = reinterpret_cast<uint32_t*>(v);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                float v[32];
-                tmem_ld32(t_lane + kPfKeys + c * 32, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] *= alpha;
-                tmem_st32(t_lane + kPfKeys + c * 32, v);
+                for (int c = 0; c < kPfKeys / 32; ++c)
+                    asm volatile(
+                        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+                        "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+                        "[%32];"
+                        : "=r"(u[32 * c + 0]), "=r"(u[32 * c + 1]), "=r"(u[32 * c + 2]), "=r"(u[32 * c + 3]),
+                          "=r"(u[32 * c + 4]), "=r"(u[32 * c + 5]), "=r"(u[32 * c + 6]), "=r"(u[32 * c + 7]),
+                          "=r"(u[32 * c + 8]), "=r"(u[32 * c + 9]), "=r"(u[32 * c + 10]), "=r"(u[32 * c + 11]),
+                          "=r"(u[32 * c + 12]), "=r"(u[32 * c + 13]), "=r"(u[32 * c + 14]), "=r"(u[32 * c + 15]),
+                          "=r"(u[32 * c + 16]), "=r"(u[32 * c + 17]), "=r"(u[32 * c + 18]), "=r"(u[32 * c + 19]),
+                          "=r"(u[32 * c + 20]), "=r"(u[32 * c + 21]), "=r"(u[32 * c + 22]), "=r"(u[32 * c + 23]),
+                          "=r"(u[32 * c + 24]), "=r"(u[32 * c + 25]), "=r"(u[32 * c + 26]), "=r"(u[32 * c + 27]),
+                          "=r"(u[32 * c + 28]), "=r"(u[32 * c + 29]), "=r"(u[32 * c + 30]), "=r"(u[32 * c + 31])
+                        : "r"(t_s + c * 32)
+                        : "memory");
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
             }
-            tmem_wait_st();
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
+            // only tiles that reach past the first row's position need the causal mask
+            const bool masked = k0 + kPfKeys - 1 > pos0 || !row_ok;
+            if (masked) {
+#pragma unroll
+                for (int i = 0; i < kPfKeys; ++i) v[i] = k0 + i <= qpos ? v[i] : NEG_INF;
+            }
+            float m_tile = NEG_INF;
+#pragma unroll
+            for (int i = 0; i < kPfKeys; ++i) m_tile = fmaxf(m_tile, v[i]);
+            m_tile *= p.scale_log2;
+            float m_new = m_ref;
+            if (j == 0 || m_tile > m_ref + 8.f) m_new = fmaxf(m_ref, m_tile);
+            const float m_use = m_new == NEG_INF ? 0.f : m_new;
+            const float alpha = (j == 0 || m_new == m_ref) ? 1.f : fast_exp2(m_ref - m_new);
+            l *= alpha;
+            m_ref = m_new;
+            // P and O are free once PV_{j-1} is done
+            if (j > 0) ok = waited(pvbar0 + 8 * ((j - 1) & 1), (uint32_t)(((j - 1) >> 1) & 1)) && ok;
             tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < NT; ++ks) {
-                const uint32_t aoff = (ks >> 2) * kRegion + (ks & 3) * 32;
-                const uint64_t vdesc = umma_desc(sV + ks * 16 * 128, kRegion, 1024);
-                umma_f16(tmem + kPfKeys, umma_desc(sPh + aoff, 16, 1024), vdesc, idesc_o, (j > 0 || ks > 0));
-                umma_f16(tmem + kPfKeys, umma_desc(sPl + aoff, 16, 1024), vdesc, idesc_o, 1u);
+            for (int c = 0; c < kPfKeys / 32; ++c) {
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const float p0 = fast_exp2(fmaf(v[32 * c + i], p.scale_log2, -m_use));
+                    const float p1 = fast_exp2(fmaf(v[32 * c + i + 1], p.scale_log2, -m_use));
+                    l += p0 + p1;
+                    hi[i / 2] = Mma<T>::pack(p0, p1);
+                    const float2 f = Mma<T>::unpack(hi[i / 2]);
+                    lo[i / 2] = Mma<T>::pack(p0 - f.x, p1 - f.y);
+                }
+                const uint32_t row_off = (uint32_t)(c >> 1) * kRegion + (uint32_t)r * 128;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t unit = (uint32_t)((c & 1) * 4 + u) ^ (uint32_t)(r & 7);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sPh + row_off + unit * 16),
+                                 "r"(hi[4 * u]), "r"(hi[4 * u + 1]), "r"(hi[4 * u + 2]), "r"(hi[4 * u + 3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sPl + row_off + unit * 16),
+                                 "r"(lo[4 * u]), "r"(lo[4 * u + 1]), "r"(lo[4 * u + 2]), "r"(lo[4 * u + 3])
+                                 : "memory");
+                }
             }
-            umma_commit(pvbar);
-            // the next tile's K and V overwrite this tile's once the products are done
-            ok = waited(pvbar, ph) && ok;
-            if (ok && j + 1 < ntiles) issue_tile(j + 1);
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(t_lane + col_o + c * 32, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                    tmem_st32(t_lane + col_o + c * 32, o);
+                }
+                tmem_wait_st();
+            }
+            // V rows past the context may hold anything (even NaN): zero them before they meet P = 0
+            const int nvalid = min(kPfKeys, ctx - k0);
+            if (nvalid < kPfKeys) {
+                ok = waited(vbar0 + 8 * (j & 1), (uint32_t)((j >> 1) & 1)) && ok;
+                const uint32_t vb = sV0 + (uint32_t)(j & 1) * kTile;
+                for (int rr = nvalid + warp; rr < kPfKeys; rr += 4)
+                    for (int dh = 0; dh < DH; ++dh)
+                        if (lane < 8)
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vb + dh * kRegion +
+                                                                                          rr * 128 + lane * 16),
+                                         "r"(0)
+                                         : "memory");
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(pready);
+            if (*abort_flag) break;
         }
-        ok = __syncthreads_and(ok);
-    }
-    if (ok) ok = waited(pvbar, (uint32_t)((ntiles - 1) & 1));
-    else mbar_wait_bounded(pvbar, (uint32_t)((ntiles - 1) & 1), nullptr, 1000000ull);  // let issued work land
-    if (!ok) {
-        if (tid == 0) {
-            flag_error(p.err, PA_DEV_ERR_TIMEOUT);
-            *abort_flag = 1;
-        }
-    } else {
-        tc_fence_after();
-        const float inv = 1.f / l;
-        const size_t orow = ((size_t)(qs + tok0 + qtok) * p.H_q + (size_t)g * p.G + (r % p.G)) * D;
+        const int jl = ntiles - 1;
+        if (ok) ok = waited(pvbar0 + 8 * (jl & 1), (uint32_t)((jl >> 1) & 1));
+        if (ok) {
+            tc_fence_after();
+            const float inv = 1.f / l;
+            const size_t orow = ((size_t)(qs + tok0 + qtok) * p.H_q + (size_t)g * p.G + (r % p.G)) * D;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            float v[32];
-            tmem_ld32(t_lane + kPfKeys + c * 32, v);
-            if (row_ok) {
-                if (p.out_dtype == PA_F32) {
-                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow + c * 32);
+            for (int c = 0; c < D / 32; ++c) {
+                float o[32];
+                tmem_ld32(t_lane + col_o + c * 32, o);
+                if (row_ok) {
+                    if (p.out_dtype == PA_F32) {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow + c * 32);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
-                } else {
-                    T* dst = static_cast<T*>(p.out) + orow + c * 32;
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                                                 o[4 * i + 3] * inv);
+                    } else {
+                        T* dst = static_cast<T*>(p.out) + orow + c * 32;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) dst[i] = from_float<T>(v[i] * inv);
+                        for (int i = 0; i < 32; ++i) dst[i] = from_float<T>(o[i] * inv);
+                    }
                 }
             }
         }
     }
     tc_fence_before();
-    __syncthreads();
+    ok = __syncthreads_and(ok && !*abort_flag);
+    if (!ok) {
+        if (tid == 0) flag_error(p.err, PA_DEV_ERR_TIMEOUT);
+        // let issued tensor-core and copy work land before the memory it uses is released
+        if (tid == 0) {
+            const int jl = ntiles - 1;
+            mbar_wait_bounded(pvbar0 + 8 * (jl & 1), (uint32_t)((jl >> 1) & 1), nullptr, 1000000ull);
+        }
+        __syncthreads();
+    }
     if (warp == 0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
@@ -395,7 +444,7 @@ static EncodeTiledFn pf_encode_fn() {
 
 static size_t prefill_smem_bytes(int D) {
     const int DH = D / 64;
-    return 1024 + (size_t)(3 * DH + 4) * kRegion + 64;
+    return 1024 + (size_t)(5 * DH + 4) * kRegion + 96;  // Q, K[2], V[2], P_hi, P_lo, barriers
 }
 
 template <typename T, int D>
