@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--seqs", type=int, default=256,
                     help="sequences (256 is the benchmarked workload; fewer for small profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--measure", choices=["decode", "swap", "prefill"], default="decode",
+    ap.add_argument("--measure", choices=["decode", "swap", "prefill", "configs"], default="decode",
                     help="swap: pa_swap_blocks device<->pinned host; prefill: chunked paged prefill (tcgen05)")
     return ap.parse_args()
 
@@ -601,6 +601,122 @@ def run_prefill(args):
     return 0
 
 
+def _time_decode(fn, att_ev, reps=20, warm=3):
+    """Median event time of a decode call and of its attention kernel (seconds)."""
+    import torch
+
+    for _ in range(warm):
+        fn(None)
+    torch.cuda.synchronize()
+    ts, ta = [], []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn(att_ev)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e-3)
+        ta.append(att_ev[0].elapsed_time(att_ev[1]) * 1e-3)
+    return float(np.median(ts)), float(np.median(ta))
+
+
+def run_configs(args):
+    """Decode throughput on the other workloads: OPT-13B MHA, the copy-on-write parallel-sampling batch
+    (logical and unique K/V bytes) and the Yi-34B-shaped 32K context, paged at B = 8 / 16 / 32 and in the
+    contiguous per-request layout (the unpaged comparison).  One JSON line per workload."""
+    import torch
+
+    import paged_kv_cache_302_gb300 as pa
+
+    torch.cuda.set_device(0)
+    hbm, _ = peaks()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+
+    def paged_case(w, alloc_fn=None):
+        a = pa.BlockAllocator(w.NB, w.B, w.free_order)
+        if alloc_fn is None:
+            for s in range(w.N):
+                a.add_seq(s)
+                a.append_slots(s, int(w.ctx[s]))
+        else:
+            alloc_fn(a)
+        tables, ctx = a.block_tables(list(range(w.N)), w.max_blocks_per_seq())
+        dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
+        pool = torch.empty((w.NB, w.B, 2, w.H_kv, w.D), dtype=dt, device="cuda").normal_()
+        q = torch.empty((w.N, w.H_q, w.D), dtype=dt, device="cuda").normal_()
+        out = torch.empty((w.N, w.H_q, w.D), device="cuda")
+        tab, cx = torch.from_numpy(tables).cuda(), torch.from_numpy(ctx).cuda()
+        ws = torch.empty(pa.pa_decode_workspace_bytes(w.N, w.H_q, w.H_kv, w.D, int(ctx.max()), 0), dtype=torch.uint8,
+                         device="cuda")
+        return a, tables, ctx, pool, q, out, tab, cx, ws
+
+    def line(name, nbytes, t_step, t_att, **extra):
+        print(json.dumps({"measure": "decode_workload", "workload": name, "unit": "GB/s",
+                          "kv_bytes": nbytes, "step_gbs": nbytes / t_step / 1e9, "attend_gbs": nbytes / t_att / 1e9,
+                          "attend_frac_of_hbm": nbytes / t_att / 1e9 / hbm, "us_per_call": t_step * 1e6, **extra}),
+              flush=True)
+
+    # OPT-13B-shaped MHA
+    w = W.opt13b()
+    a, tables, ctx, pool, q, out, tab, cx, ws = paged_case(w)
+    nbytes = int(ctx.astype(np.int64).sum()) * 2 * w.H_kv * w.D * 2
+    t, ta = _time_decode(lambda e: pa.pa_decode(out, q, pool, tab, cx, int(ctx.max()), workspace=ws, dev_err=err,
+                                                attend_events=e), ev)
+    line("opt13b_mha_fp16", nbytes, t, ta)
+
+    # parallel sampling with copy-on-write prefix sharing
+    w = W.cow()
+
+    def cow_alloc(a):
+        for pidx in range(w.prompts):
+            base = pidx * w.samples
+            a.add_seq(base)
+            a.append_slots(base, w.prompt_len)
+            for j in range(1, w.samples):
+                a.fork(base, base + j)
+        a.append_batch(list(range(w.N)), w.extra)
+
+    a, tables, ctx, pool, q, out, tab, cx, ws = paged_case(w, cow_alloc)
+    per_tok = 2 * w.H_kv * w.D * 2
+    logical = int(ctx.astype(np.int64).sum()) * per_tok
+    uniq = len(set(tables[tables >= 0].tolist())) * w.B * per_tok
+    t, ta = _time_decode(lambda e: pa.pa_decode(out, q, pool, tab, cx, int(ctx.max()), workspace=ws, dev_err=err,
+                                                attend_events=e), ev)
+    line("cow_parallel_sampling", logical, t, ta, unique_kv_bytes=uniq, attend_unique_gbs=uniq / ta / 1e9,
+         attend_unique_frac_of_hbm=uniq / ta / 1e9 / hbm)
+
+    # Yi-34B-shaped long context, paged at three block sizes and contiguous
+    for B in (8, 16, 32):
+        w = W.yi34b_long(B=B)
+        a, tables, ctx, pool, q, out, tab, cx, ws = paged_case(w)
+        nbytes = int(ctx.astype(np.int64).sum()) * 2 * w.H_kv * w.D * 2
+        t, ta = _time_decode(lambda e: pa.pa_decode(out, q, pool, tab, cx, int(ctx.max()), workspace=ws,
+                                                    dev_err=err, attend_events=e), ev)
+        res = dict(paged_step_gbs=nbytes / t / 1e9, paged_attend_gbs=nbytes / ta / 1e9)
+        # the same K/V in per-request buffers at request offsets req * S
+        N_max, S_max = w.N, int(ctx.max())
+        req = torch.from_numpy(W.request_ids(w, N_max)).cuda()
+        t_idx = torch.arange(S_max, device="cuda")
+        kb = torch.empty((N_max, S_max, w.H_kv, w.D), dtype=torch.bfloat16, device="cuda")
+        vb = torch.empty_like(kb)
+        for si in range(w.N):
+            phys = tab[si, t_idx // B].long()
+            kb[req[si]] = pool[phys, t_idx % B, 0]
+            vb[req[si]] = pool[phys, t_idx % B, 1]
+        out2 = torch.empty_like(out)
+        tc, tca = _time_decode(lambda e: pa.pa_decode_contiguous(out2, q, kb, vb, req, cx, int(ctx.max()),
+                                                                 workspace=ws, dev_err=err, attend_events=e), ev)
+        torch.cuda.synchronize()
+        assert torch.equal(out, out2), "paged and contiguous outputs differ"
+        line(f"yi34b_long_B{B}", nbytes, t, ta, contiguous_step_gbs=nbytes / tc / 1e9,
+             contiguous_attend_gbs=nbytes / tca / 1e9, paged_over_contiguous_step=tc / t,
+             paged_over_contiguous_attend=tca / ta)
+        del kb, vb, pool
+    assert int(err.item()) == 0
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -609,6 +725,8 @@ def main():
         return run_swap(args)
     if args.measure == "prefill":
         return run_prefill(args)
+    if args.measure == "configs":
+        return run_configs(args)
     return run_ours(args)
 
 
