@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--seqs", type=int, default=256,
                     help="sequences (256 is the benchmarked workload; fewer for small profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--measure", choices=["decode", "swap", "prefill", "configs"], default="decode",
+    ap.add_argument("--measure", choices=["decode", "swap", "prefill", "configs", "vmm"], default="decode",
                     help="swap: pa_swap_blocks device<->pinned host; prefill: chunked paged prefill (tcgen05)")
     return ap.parse_args()
 
@@ -717,6 +717,48 @@ def run_configs(args):
     return 0
 
 
+def run_vmm(args):
+    """Virtually contiguous KV: time to map physical pages on demand (per 2 MB page, create + map + access)
+    and decode over the mapped buffers, Yi-34B-shaped 8 x 32K context."""
+    import torch
+
+    import paged_kv_cache_302_gb300 as pa
+
+    torch.cuda.set_device(0)
+    N, ctx_len, H_q, H_kv, D = 8, 32768, 56, 8, 128
+    V = pa.VirtualKV(1, N, ctx_len, H_kv, D)
+    reqs = [V.alloc_reqid() for _ in range(N)]
+    t0 = time.perf_counter()
+    V.step(reqs, [ctx_len] * N)
+    t_map = time.perf_counter() - t0
+    pages = sum(V.mapped_pages(r) for r in reqs) * 2        # K and V buffers
+    # fill with N(0,1) through the contiguous cache write, then decode
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for r in reqs:
+        k = torch.empty((ctx_len, H_kv, D), dtype=torch.bfloat16, device="cuda").normal_()
+        pa.pa_write_contiguous(k, k, V.k_ptrs[0], V.v_ptrs[0], torch.full((ctx_len,), r, dtype=torch.int32,
+                                                                            device="cuda"),
+                               torch.arange(ctx_len, dtype=torch.int32, device="cuda"), N, V.S, dev_err=err)
+    q = torch.empty((N, H_q, D), dtype=torch.bfloat16, device="cuda").normal_()
+    out = torch.empty((N, H_q, D), device="cuda")
+    req_t = torch.tensor(reqs, dtype=torch.int32, device="cuda")
+    ctx_t = torch.full((N,), ctx_len, dtype=torch.int32, device="cuda")
+    ws = torch.empty(pa.pa_decode_workspace_bytes(N, H_q, H_kv, D, ctx_len, 0), dtype=torch.uint8, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+    t, ta = _time_decode(lambda e: pa.pa_decode_contiguous_raw(out, q, V.k_ptrs[0], V.v_ptrs[0], req_t, ctx_t, N, V.S,
+                                                               H_kv, ctx_len, workspace=ws, dev_err=err,
+                                                               attend_events=e), ev)
+    assert int(err.item()) == 0
+    nbytes = N * ctx_len * 2 * H_kv * D * 2
+    hbm, _ = peaks()
+    print(json.dumps({"measure": "vkv", "page_bytes": V.page_bytes, "pages_mapped": pages,
+                      "us_per_page_create_map_access": t_map / pages * 1e6, "decode_attend_gbs": nbytes / ta / 1e9,
+                      "decode_attend_frac_of_hbm": nbytes / ta / 1e9 / hbm, "tokens_per_page_per_buffer":
+                      V.page_bytes // (H_kv * D * 2)}), flush=True)
+    V.close()
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -727,6 +769,8 @@ def main():
         return run_prefill(args)
     if args.measure == "configs":
         return run_configs(args)
+    if args.measure == "vmm":
+        return run_vmm(args)
     return run_ours(args)
 
 

@@ -222,6 +222,52 @@ pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const void* q, const
                              pa_dtype kv_dtype, int* dev_err, void* const* attend_events, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Cache write for the contiguous per-request layout ([VA] リクエスト単位のKV
+ * キャッシュインデキシング: request r's cache starts at r * S).
+ * k, v: [T][H_kv][D]; k_buf, v_buf: [N_max][S_max][H_kv][D].  Token i's rows go
+ * to request req_ids[i] at position positions[i]; req_ids[i] < 0 skips the
+ * token; a request id >= N_max is flagged PA_DEV_ERR_REQ and a position
+ * outside [0, S_max) PA_DEV_ERR_SLOT (both skipped).  With pa_vkv buffers the
+ * position must lie inside the pages pa_vkv_step has mapped.
+ * ---------------------------------------------------------------------- */
+pa_status pa_write_contiguous(const void* k, const void* v, void* k_buf, void* v_buf, const int32_t* req_ids,
+                              const int32_t* positions, int T, int N_max, int S_max, int H_kv, int D, pa_dtype dtype,
+                              int* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Virtually contiguous KV buffers with physical pages mapped on demand
+ * ([VA] 技術的詳細: reserve the virtual range up front with cuMemAddressReserve,
+ * back it with physical pages through cuMemCreate + cuMemMap as contexts grow;
+ * 実装のポイント: the init / alloc_reqid / step / free_reqid interface; free
+ * keeps the pages mapped for the slot's next owner, the explainer's deferred
+ * reclamation).  Page size is the driver's minimum granularity (2 MB on this
+ * hardware; the explainer's 64 KB pages need a modified driver and are not
+ * used).  Buffers of layer l: K and V, each [max_batch][S][H_kv][D] where
+ * S = *S_tokens >= max_ctx (a whole number of pages per request); pass
+ * N_max = max_batch and S_max = S to pa_decode_contiguous / pa_write_contiguous.
+ * Host calls, one device (the device current at create); not thread-safe.
+ * - pa_vkv_create reserves 2 * num_layers ranges, maps nothing.
+ * - pa_vkv_alloc_reqid picks a free request slot (one that still has pages
+ *   first); PA_ERR_OOM when all max_batch are taken.
+ * - pa_vkv_step maps pages so request req_ids[i] covers ctx_lens[i] tokens
+ *   (rounded up to 32, the decode kernel's read granule) in every buffer; a
+ *   request whose pages cannot be created is left as it was and PA_ERR_OOM
+ *   returned (requests before it in the list keep their new pages).
+ * - pa_vkv_free_reqid releases the slot, not its pages; pa_vkv_reclaim unmaps
+ *   the pages of every free slot.
+ * ---------------------------------------------------------------------- */
+pa_status pa_vkv_create(int num_layers, int max_batch, int max_ctx, int H_kv, int D, pa_dtype dtype, void** out);
+void pa_vkv_destroy(void* vkv);
+/* k_bufs, v_bufs: [num_layers] device pointers (nullable); S_tokens: request stride in tokens;
+ * page_bytes: physical page size. */
+pa_status pa_vkv_info(void* vkv, void** k_bufs, void** v_bufs, int64_t* S_tokens, int64_t* page_bytes);
+pa_status pa_vkv_alloc_reqid(void* vkv, int* req_id);
+pa_status pa_vkv_step(void* vkv, const int32_t* req_ids, const int32_t* ctx_lens, int n);
+pa_status pa_vkv_free_reqid(void* vkv, int req_id);
+pa_status pa_vkv_reclaim(void* vkv);
+pa_status pa_vkv_mapped_pages(void* vkv, int req_id, int* pages);
+
+/* ------------------------------------------------------------------------
  * Merge of split-context partials (the running maximum / exponential sum /
  * unnormalised output the block-by-block online softmax keeps, [PA]
  * アルゴリズムの擬似コード, taken per partition and combined).

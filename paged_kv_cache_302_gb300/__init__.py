@@ -83,6 +83,15 @@ def _declare(L):
         "pa_alloc_append_batch": ([P, i32, P, P, P, P, i32, P, P, i32, P], i32),
         "pa_update_block_tables": ([P, i32, i32, P, i32, P, P], i32),
         "pa_swap_blocks": ([P, i32, P, i32, P, i32, i32, i32, i32, i32, P, P], i32),
+        "pa_write_contiguous": ([P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, P], i32),
+        "pa_vkv_create": ([i32, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_void_p)], i32),
+        "pa_vkv_destroy": ([P], None),
+        "pa_vkv_info": ([P, P, P, P, P], i32),
+        "pa_vkv_alloc_reqid": ([P, P], i32),
+        "pa_vkv_step": ([P, P, P, i32], i32),
+        "pa_vkv_free_reqid": ([P, i32], i32),
+        "pa_vkv_reclaim": ([P], i32),
+        "pa_vkv_mapped_pages": ([P, i32, P], i32),
         "pa_prefill": ([P, i32, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, P, P], i32),
         "pa_alloc_fork": ([P, i32, i32], i32),
         "pa_alloc_free_seq": ([P, i32], i32),
@@ -336,6 +345,93 @@ def pa_prefill(out, q, pool, block_tables, ctx_lens, q_start, max_q_len, scale=N
                         _dev(block_tables, "block_tables", torch.int32), _dev(ctx_lens, "ctx_lens", torch.int32),
                         _dev(q_start, "q_start", torch.int32), N, T, H_q, H_kv, D, B, MB, NB, int(max_q_len), scale,
                         _dtype_code(pool.dtype), _err_ptr(dev_err), _stream_ptr(stream)))
+    return out
+
+
+def pa_write_contiguous(k, v, k_ptr, v_ptr, req_ids, positions, N_max, S_max, dev_err=None, stream=None):
+    """Write k, v [T, H_kv, D] into contiguous buffers (device pointers or tensors [N_max, S_max, H_kv, D])."""
+    T, H_kv, D = k.shape
+
+    def ptr(x):
+        return _dev(x, "buffer") if isinstance(x, torch.Tensor) else ctypes.c_void_p(int(x))
+
+    L = load()
+    _check(L.pa_write_contiguous(_dev(k, "k"), _dev(v, "v", k.dtype), ptr(k_ptr), ptr(v_ptr),
+                                 _dev(req_ids, "req_ids", torch.int32), _dev(positions, "positions", torch.int32), T,
+                                 int(N_max), int(S_max), H_kv, D, _dtype_code(k.dtype), _err_ptr(dev_err),
+                                 _stream_ptr(stream)))
+
+
+class VirtualKV:
+    """pa_vkv_*: virtually contiguous K/V buffers backed by physical pages on demand."""
+
+    def __init__(self, num_layers, max_batch, max_ctx, H_kv, D, dtype=torch.bfloat16):
+        self._L = load()
+        self._h = ctypes.c_void_p()
+        _check(self._L.pa_vkv_create(num_layers, max_batch, max_ctx, H_kv, D, _dtype_code(dtype),
+                                     ctypes.byref(self._h)))
+        self.layers, self.max_batch, self.H_kv, self.D, self.dtype = num_layers, max_batch, H_kv, D, dtype
+        k = (ctypes.c_void_p * num_layers)()
+        v = (ctypes.c_void_p * num_layers)()
+        S = ctypes.c_int64()
+        page = ctypes.c_int64()
+        _check(self._L.pa_vkv_info(self._h, k, v, ctypes.byref(S), ctypes.byref(page)))
+        self.k_ptrs = [int(x) for x in k]
+        self.v_ptrs = [int(x) for x in v]
+        self.S = S.value
+        self.page_bytes = page.value
+
+    def alloc_reqid(self) -> int:
+        r = ctypes.c_int()
+        _check(self._L.pa_vkv_alloc_reqid(self._h, ctypes.byref(r)))
+        return r.value
+
+    def step(self, req_ids, ctx_lens):
+        import numpy as np
+        ids = np.ascontiguousarray(req_ids, dtype=np.int32)
+        cx = np.ascontiguousarray(ctx_lens, dtype=np.int32)
+        _check(self._L.pa_vkv_step(self._h, _i32p(ids), _i32p(cx), len(ids)))
+
+    def free_reqid(self, r: int):
+        _check(self._L.pa_vkv_free_reqid(self._h, int(r)))
+
+    def reclaim(self):
+        _check(self._L.pa_vkv_reclaim(self._h))
+
+    def mapped_pages(self, r: int) -> int:
+        n = ctypes.c_int()
+        _check(self._L.pa_vkv_mapped_pages(self._h, int(r), ctypes.byref(n)))
+        return n.value
+
+    def close(self):
+        if self._h:
+            self._L.pa_vkv_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def pa_decode_contiguous_raw(out, q, k_ptr: int, v_ptr: int, req_ids, ctx_lens, N_max, S_max, H_kv, max_ctx,
+                             scale=None, partition_tokens=0, workspace=None, dev_err=None, attend_events=None,
+                             stream=None):
+    """pa_decode_contiguous over raw device buffers [N_max, S_max, H_kv, D] of q's dtype (e.g. VirtualKV's)."""
+    N, H_q, D = q.shape
+    if tuple(out.shape) != (N, H_q, D):
+        raise PAError(PA_ERR_INVALID, "shape mismatch")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    nbytes = pa_decode_workspace_bytes(N, H_q, H_kv, D, int(max_ctx), partition_tokens)
+    ws = _workspace(workspace, nbytes, q.device)
+    L = load()
+    _check(L.pa_decode_contiguous(_dev(out, "out"), _dtype_code(out.dtype), _dev(q, "q"), ctypes.c_void_p(int(k_ptr)),
+                                  ctypes.c_void_p(int(v_ptr)), _dev(req_ids, "req_ids", torch.int32),
+                                  _dev(ctx_lens, "ctx_lens", torch.int32), N, H_q, H_kv, D, int(N_max), int(S_max),
+                                  int(max_ctx), scale, int(partition_tokens), _dev(ws, "workspace"),
+                                  ws.numel() * ws.element_size(), _dtype_code(q.dtype), _err_ptr(dev_err),
+                                  _events_arg(attend_events, stream), _stream_ptr(stream)))
     return out
 
 

@@ -12,7 +12,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libpa.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["decode.cu", "prefill.cu", "cache_ops.cu", "capi.cpp", "alloc.cpp", "static_ws.cu"]
+SOURCES = ["decode.cu", "prefill.cu", "cache_ops.cu", "capi.cpp", "alloc.cpp", "vkv.cpp", "static_ws.cu"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 

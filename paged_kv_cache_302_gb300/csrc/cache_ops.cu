@@ -176,4 +176,47 @@ pa_status launch_swap_blocks(void* dst, int NB_dst, const void* src, int NB_src,
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "swap_blocks launch");
 }
 
+// Cache write for the contiguous per-request layout: token i's K and V rows go to
+// request req_ids[i] at position positions[i] (offset (req * S + pos) rows).
+__global__ void __launch_bounds__(128) write_contiguous_kernel(const uint4* __restrict__ k,
+                                                               const uint4* __restrict__ v, uint4* __restrict__ kbuf,
+                                                               uint4* __restrict__ vbuf,
+                                                               const int32_t* __restrict__ req_ids,
+                                                               const int32_t* __restrict__ pos, int T, int N_max,
+                                                               int S, int row_vec, int* err) {
+    griddep_wait();
+    griddep_launch_dependents();
+    for (int i = blockIdx.x; i < T; i += gridDim.x) {
+        const int r = req_ids[i], t = pos[i];
+        if (r < 0) continue;  // padding
+        if (r >= N_max || t < 0 || t >= S) {
+            if (threadIdx.x == 0) flag_error(err, r >= N_max ? PA_DEV_ERR_REQ : PA_DEV_ERR_SLOT);
+            continue;
+        }
+        const int64_t row = ((int64_t)r * S + t) * row_vec;
+        const uint4* sk = k + (int64_t)i * row_vec;
+        const uint4* sv = v + (int64_t)i * row_vec;
+        for (int e = threadIdx.x; e < row_vec; e += blockDim.x) {
+            const uint4 a = sk[e];
+            const uint4 b = sv[e];
+            kbuf[row + e] = a;
+            vbuf[row + e] = b;
+        }
+    }
+}
+
+pa_status launch_write_contiguous(const void* k, const void* v, void* k_buf, void* v_buf, const int32_t* req_ids,
+                                  const int32_t* positions, int T, int N_max, int S, int H_kv, int D, int* dev_err,
+                                  cudaStream_t stream) {
+    if (T == 0) return PA_OK;
+    const int row_vec = H_kv * D * 2 / 16;
+    const int grid = T < 152 * 16 ? T : 152 * 16;
+    cudaError_t e = launch_kernel(write_contiguous_kernel, dim3(grid), dim3(128), 0, stream,
+                                  static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+                                  static_cast<uint4*>(k_buf), static_cast<uint4*>(v_buf), req_ids, positions, T, N_max,
+                                  S, row_vec, dev_err);
+    count_launch();
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "write_contiguous launch");
+}
+
 }  // namespace pa

@@ -130,6 +130,21 @@ pa_status pa_swap_blocks(void* dst_pool, int NB_dst, const void* src_pool, int N
                               static_cast<cudaStream_t>(stream));
 }
 
+pa_status pa_write_contiguous(const void* k, const void* v, void* k_buf, void* v_buf, const int32_t* req_ids,
+                              const int32_t* positions, int T, int N_max, int S_max, int H_kv, int D, pa_dtype dtype,
+                              int* dev_err, void* stream) {
+    g_msg[0] = 0;
+    if (!kv_dtype_ok(dtype)) return fail(PA_ERR_UNSUPPORTED, "dtype must be F16 or BF16");
+    if (T < 0 || N_max <= 0 || S_max <= 0 || H_kv <= 0 || D <= 0) return fail(PA_ERR_INVALID, "bad sizes");
+    if ((H_kv * D) % 8) return fail(PA_ERR_UNSUPPORTED, "H_kv * D must be a multiple of 8");
+    if (T == 0) return PA_OK;
+    if (!k || !v || !k_buf || !v_buf || !req_ids || !positions) return fail(PA_ERR_INVALID, "null pointer");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_buf) || !aligned16(v_buf))
+        return fail(PA_ERR_INVALID, "k, v and the buffers must be 16-byte aligned");
+    return launch_write_contiguous(k, v, k_buf, v_buf, req_ids, positions, T, N_max, S_max, H_kv, D, dev_err,
+                                   static_cast<cudaStream_t>(stream));
+}
+
 pa_status pa_update_block_tables(int32_t* tables, int N, int MB, const int32_t* updates, int n, int* dev_err,
                                  void* stream) {
     g_msg[0] = 0;

@@ -19,6 +19,9 @@ void count_launch();
 
 pa_status launch_reshape_and_cache(const void* k, const void* v, void* pool, const int64_t* slot_mapping, int T,
                                    int NB, int B, int H_kv, int D, int* dev_err, cudaStream_t stream);
+pa_status launch_write_contiguous(const void* k, const void* v, void* k_buf, void* v_buf, const int32_t* req_ids,
+                                  const int32_t* positions, int T, int N_max, int S, int H_kv, int D, int* dev_err,
+                                  cudaStream_t stream);
 pa_status launch_swap_blocks(void* dst, int NB_dst, const void* src, int NB_src, const int64_t* pairs, int n,
                              int64_t blk_bytes, int* dev_err, cudaStream_t stream);
 pa_status launch_update_tables(int32_t* tables, int N, int MB, const int32_t* updates, int n, int* dev_err,
