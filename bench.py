@@ -60,6 +60,21 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def whole_job(t_local: float, bytes_local: float, device):
+    """Whole-job figures of independent replicas: the slowest rank's time and the sum of all ranks' bytes
+    (a plain pass-through on one process)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(t_local), float(bytes_local)
+    t = torch.tensor([float(t_local)], dtype=torch.float64, device=device)
+    b = torch.tensor([float(bytes_local)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(b.item())
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -354,16 +369,7 @@ def run_ours(args):
     attend_s = [att_ev[i][0].elapsed_time(att_ev[i][1]) * 1e-3 for i in range(args.warmup, nsteps)]
     assert int(err.item()) == 0, f"device error flags {int(err.item())}"
     timed_bytes = sum(step_bytes[args.warmup:])
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([t_dev], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_dev = float(tt.item())
-        bb = torch.tensor([float(timed_bytes)], device=dev)
-        dist.all_reduce(bb)
-        total_bytes = float(bb.item())
-    else:
-        total_bytes = float(timed_bytes)
+    t_dev, total_bytes = whole_job(t_dev, timed_bytes, dev)
     value = total_bytes / t_dev / 1e9
     ms_per_step = t_dev / args.steps * 1e3
 
@@ -500,15 +506,8 @@ def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world, tab
         e2e_bytes.append(nbytes)
     t_e2e = time.perf_counter() - t0
     assert int(err.item()) == 0, f"device error flags {int(err.item())}"
-    e2e_value = sum(e2e_bytes) / t_e2e / 1e9
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([t_e2e, float(sum(e2e_bytes))], device=dev)
-        mx = tt[:1].clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        sm = tt[1:].clone()
-        dist.all_reduce(sm)
-        e2e_value = float(sm.item()) / float(mx.item()) / 1e9
+    t_e2e, e2e_total = whole_job(t_e2e, sum(e2e_bytes), dev)
+    e2e_value = e2e_total / t_e2e / 1e9
     return e2e_value, int(round(sum(h2d_bytes) / len(h2d_bytes))), d2h
 
 
