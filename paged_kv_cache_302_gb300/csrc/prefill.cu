@@ -32,10 +32,12 @@
 
 namespace pa {
 
-constexpr int kPfRows = 128;     // query rows per CTA (tcgen05 M)
+constexpr int kPfRows = 128;     // query rows per query tile (tcgen05 M); a CTA owns two query tiles
 constexpr int kPfKeys = 128;     // keys per tile (tcgen05 N of S, K of P V)
-constexpr int kPfThreads = 192;  // warps 0-3: one thread per row / TMEM lane; 4: TMA; 5: MMA
-constexpr uint32_t kTmemCols = 512;  // S[0], S[1] (128 columns each), O (D columns)
+constexpr int kPfSoftmaxThreads = 256;  // two warpgroups, one per query tile: one thread per row / TMEM lane
+constexpr int kPfThreads = kPfSoftmaxThreads + 64;  // + warp 8: TMA, warp 9: MMA
+constexpr int kPfStages = 2;     // K and V stages in shared memory
+constexpr uint32_t kTmemCols = 512;  // S/P of query tiles 0, 1 (128 columns each), then O_0, O_1 (D columns each)
 constexpr uint32_t kRegion = kPfRows * 128;  // one [128 rows][64 columns] 16-bit swizzled region: 16 KB
 
 struct PrefillParams {
@@ -74,6 +76,16 @@ __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t a, uint64_t b
         "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
         "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// Same, with the A operand (M rows x 16 k, two 16-bit elements per 32-bit column) read from TMEM.
+__device__ __forceinline__ void umma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                            uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
 
@@ -119,49 +131,114 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ----------------------------------------------------------------------------- packed fp32 pairs
+
+// d = a * b + c on two fp32 lanes at once (PTX fma.rn.f32x2).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Barrier 1 over the softmax warpgroups; returns the AND of `pred` over them.
+__device__ __forceinline__ bool softmax_bar_and(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "n"(kPfSoftmaxThreads)
+        : "memory");
+    return r != 0;
+}
 
 // ----------------------------------------------------------------------------- kernel
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                 const __grid_constant__ CUtensorMap tm_kv,
+                                                                const __grid_constant__ CUtensorMap tm_kv_blk,
                                                                 const PrefillParams p) {
     constexpr int DH = D / 64;          // 64-column halves of a head row
     constexpr int NK = D / 16;          // k-steps of S = Q K^T
     constexpr int NT = kPfKeys / 16;    // k-steps of O += P V
+    constexpr int NS = kPfStages;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t idesc_s = umma_idesc(kBf16, kPfRows, kPfKeys, false);
     constexpr uint32_t idesc_o = umma_idesc(kBf16, kPfRows, D, true);
-    constexpr uint32_t kTile = DH * kRegion;  // one K (or V) tile: 128 keys x D
+    constexpr uint32_t kTile = DH * kRegion;  // one Q tile (128 rows x D), or one K or V tile (128 keys x D)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_addr(base);
-    // Q | K[2] | V[2] | P_hi | P_lo | barriers
-    const uint32_t sQ = sb, sK0 = sQ + kTile, sV0 = sK0 + 2 * kTile, sPh = sV0 + 2 * kTile, sPl = sPh + 2 * kRegion,
-                   sBar = sPl + 2 * kRegion;
-    // barriers: q, k[2], v[2], s[2], pv[2], p_ready
-    const uint32_t qbar = sBar, kbar0 = sBar + 8, vbar0 = sBar + 24, sbar0 = sBar + 40, pvbar0 = sBar + 56,
-                   pready = sBar + 72;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + (sBar - sb) + 80);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + (sBar - sb) + 84);
+    // Q[2] | K[NS] | V[NS] | barriers
+    const uint32_t sQ0 = sb, sK0 = sQ0 + 2 * kTile, sV0 = sK0 + NS * kTile, sBar = sV0 + NS * kTile;
+    // barriers: q; k_full, v_full, k_free, v_free [NS]; s_full, pv_done, p_ready [2] (one per query tile)
+    const uint32_t qbar = sBar, kfull0 = qbar + 8, vfull0 = kfull0 + 8 * NS, kfree0 = vfull0 + 8 * NS,
+                   vfree0 = kfree0 + 8 * NS, sfull0 = vfree0 + 8 * NS, pvd0 = sfull0 + 16, prd0 = pvd0 + 16;
+    constexpr int kBars = 1 + 4 * NS + 6;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + (sBar - sb) + 8 * kBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + (sBar - sb) + 8 * kBars + 4);
 
     griddep_wait();
     griddep_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = blockIdx.z, g = blockIdx.y;
     const int qs = p.q_start[s], q_len = p.q_start[s + 1] - qs;
-    const int tok0 = blockIdx.x * p.TQ;
+    const int tok0 = blockIdx.x * 2 * p.TQ;  // first query token of tile 0; tile 1 follows at tok0 + TQ
     if (tok0 >= q_len) return;  // uniform per CTA, before any allocation
     const int ctx = p.ctx_lens[s];
     if (q_len > ctx || ctx > p.MB * p.B || q_len < 0) {
         if (tid == 0) flag_error(p.err, PA_DEV_ERR_CTX);
         return;
     }
-    const int pos0 = ctx - q_len + tok0;                         // position of the tile's first query token
-    const int last_tok = min(tok0 + p.TQ, q_len) - 1;
-    const int nkeys = ctx - q_len + last_tok + 1;                // keys the tile's last query sees
+    const int pos0 = ctx - q_len + tok0;                         // position of the CTA's first query token
+    const int last_tok = min(tok0 + 2 * p.TQ, q_len) - 1;
+    const int nkeys = ctx - q_len + last_tok + 1;                // keys the CTA's last query sees
     const int ntiles = (nkeys + kPfKeys - 1) / kPfKeys;
+    auto st = [](int j) { return (uint32_t)(j % NS); };
+    auto ph = [](int j) { return (uint32_t)((j / NS) & 1); };
+    // With B = 8 the K and V tiles are stored block by block, [block][half][8 rows][128 bytes], and one copy
+    // brings a whole block; otherwise each tile holds one 128-key region per 64-column half, [half][128 rows][128 B]
+    // (one copy per block and half), which measured faster for the value product at B = 16 and 32.
+    const bool k_blk = p.B == 8, v_blk = p.B == 8;
+    const uint32_t blk_bytes = (uint32_t)DH * p.B * 128;
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
@@ -170,26 +247,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        for (int i = 0; i < 9; ++i) mbar_init(sBar + 8 * i, 1);
-        mbar_init(pready, kPfRows);
+        for (int i = 0; i < kBars; ++i) mbar_init(sBar + 8 * i, 1);
+        mbar_init(prd0, kPfRows);
+        mbar_init(prd0 + 8, kPfRows);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    // rows past TQ*G (when G does not divide 128) are never loaded: clear them once
-    if (warp < 4)
-        for (int r = p.TQ * p.G + warp; r < kPfRows; r += 4)
+    // rows past TQ*G (when G does not divide 128) are never loaded: clear them once in both query tiles
+    if (warp < 8)
+        for (int r = p.TQ * p.G + (warp & 3); r < kPfRows; r += 4)
             for (int dh = 0; dh < DH; ++dh)
                 if (lane < 8)
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sQ + dh * kRegion + r * 128 +
-                                                                                  lane * 16),
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sQ0 + (warp >> 2) * kTile +
+                                                                                  dh * kRegion + r * 128 + lane * 16),
                                  "r"(0)
                                  : "memory");
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;              // columns: S[0] 0..127, S[1] 128..255, O 256..
-    const uint32_t col_o = 2 * kPfKeys;
+    const uint32_t tmem = *tmem_slot;  // columns: S/P of query tile w at 128 w, O_w at 256 + D w
     auto waited = [&](uint32_t bar, uint32_t parity) {
         const bool w = mbar_wait_bounded(bar, parity, abort_flag);
         if (!w) *abort_flag = 1;
@@ -197,95 +274,130 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     };
     bool ok = true;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ TMA producer
         const uint64_t pol = policy_evict_first();
         if (lane == 0) {
-            mbar_arrive_expect_tx(qbar, (uint32_t)DH * p.G * p.TQ * 128);
-            for (int dh = 0; dh < DH; ++dh)
-                tma_load_4d(sQ + dh * kRegion, &tm_q, qbar, 0, dh, g * p.G, qs + tok0, policy_evict_normal());
+            mbar_arrive_expect_tx(qbar, (uint32_t)2 * DH * p.G * p.TQ * 128);
+            for (int w = 0; w < 2; ++w)
+                for (int dh = 0; dh < DH; ++dh)
+                    tma_load_4d(sQ0 + w * kTile + dh * kRegion, &tm_q, qbar, 0, dh, g * p.G, qs + tok0 + w * p.TQ,
+                                policy_evict_normal());
         }
-        for (int t = 0; t < ntiles && ok; ++t) {
+        // Lane b issues the copies of the tile's b-th KV block.
+        auto table_entry = [&](int t) {
             const int k0 = t * kPfKeys;
             const int nblk = min(kPfKeys, ctx - k0 + p.B - 1) / p.B;  // blocks holding keys of this tile
-            int mine = lane < nblk ? p.tables[(size_t)s * p.MB + k0 / p.B + lane] : 0;
-            if (lane < nblk && (unsigned)mine >= (unsigned)p.NB) {
+            int e = lane < nblk ? p.tables[(size_t)s * p.MB + k0 / p.B + lane] : 0;
+            if (lane < nblk && (unsigned)e >= (unsigned)p.NB) {
                 flag_error(p.err, PA_DEV_ERR_BLOCK);
-                mine = p.NB;  // past the tensor: TMA fills zeros
+                e = p.NB;  // past the tensor: TMA fills zeros
             }
+            return e;
+        };
+        int mine = table_entry(0);
+        for (int t = 0; t < ntiles && ok; ++t) {
+            const int nblk = min(kPfKeys, ctx - t * kPfKeys + p.B - 1) / p.B;
+            const int cur = mine;
+            if (t + 1 < ntiles) mine = table_entry(t + 1);  // in flight while this tile's copies are issued
             const uint32_t bytes = (uint32_t)nblk * DH * p.B * 128;
-            const uint32_t b2 = (uint32_t)(t & 1);
+            const uint32_t b = st(t);
             for (int which = 0; which < 2 && ok; ++which) {
-                // buffer t % 2 is free once S_{t-2} (for K) / PV_{t-2} (for V) is done
-                if (t >= 2) ok = waited((which ? pvbar0 : sbar0) + 8 * b2, (uint32_t)(((t - 2) >> 1) & 1));
+                // stage t % NS is free once both query tiles' S_{t-NS} (for K) / PV_{t-NS} (for V) are done
+                if (t >= NS) ok = waited((which ? vfree0 : kfree0) + 8 * b, ph(t - NS));
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                const uint32_t bar = (which ? vbar0 : kbar0) + 8 * b2;
-                const uint32_t dst = (which ? sV0 : sK0) + b2 * kTile;
+                const uint32_t bar = (which ? vfull0 : kfull0) + 8 * b;
+                const uint32_t dst = (which ? sV0 : sK0) + b * kTile;
                 if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
-                for (int b = 0; b < nblk; ++b) {
-                    const int e = __shfl_sync(0xffffffffu, mine, b);
-                    if (lane == 0)
+                __syncwarp();
+                if (lane < nblk) {
+                    if (which ? v_blk : k_blk)
+                        tma_load_5d(dst + (uint32_t)lane * blk_bytes, &tm_kv_blk, bar, 0, cur * p.B, 0, g, which, pol);
+                    else
                         for (int dh = 0; dh < DH; ++dh)
-                            tma_load_5d(dst + dh * kRegion + (uint32_t)b * p.B * 128, &tm_kv, bar, 0, e * p.B, dh, g,
-                                        which, pol);
+                            tma_load_5d(dst + dh * kRegion + (uint32_t)lane * p.B * 128, &tm_kv, bar, 0, cur * p.B, dh,
+                                        g, which, pol);
                 }
             }
-            ok = __all_sync(0xffffffffu, ok);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        auto issue_s = [&](int j) {  // S[j % 2] = Q K_j^T
-            const uint32_t kb = sK0 + (uint32_t)(j & 1) * kTile;
+        // S_w(j) = Q_w K_j^T goes to TMEM buffer w and is overwritten there by P_w(j); O_w += P_w(j) V_j.
+        // S_w(j+1) reuses the buffer once PV_w(j) has read P_w(j).
+        auto issue_s = [&](int w, int j) {
+            const uint32_t kb = sK0 + st(j) * kTile;
+            const uint32_t qb = sQ0 + w * kTile;
 #pragma unroll
             for (int ks = 0; ks < NK; ++ks) {
                 const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
-                umma_f16(tmem + (uint32_t)(j & 1) * kPfKeys, umma_desc(sQ + off, 16, 1024),
-                         umma_desc(kb + off, 16, 1024), idesc_s, ks > 0);
+                const uint64_t kdesc = k_blk ? umma_desc(kb + (ks >> 2) * 1024 + (ks & 3) * 32, 16, blk_bytes)
+                                             : umma_desc(kb + off, 16, 1024);
+                umma_f16(tmem + (uint32_t)w * kPfKeys, umma_desc(qb + off, 16, 1024), kdesc, idesc_s, ks > 0);
             }
-            umma_commit(sbar0 + 8 * (j & 1));
+            umma_commit(sfull0 + 8 * w);
+            if (w == 1) umma_commit(kfree0 + 8 * st(j));  // K_j has served both query tiles
+        };
+        auto issue_pv = [&](int w, int j) {  // O_w += P_hi V + P_lo V, P read from TMEM
+            const uint32_t vb = sV0 + st(j) * kTile;
+            const uint32_t pcol = tmem + (uint32_t)w * kPfKeys;
+            const uint32_t ocol = tmem + 2 * kPfKeys + (uint32_t)w * D;
+#pragma unroll
+            for (int ks = 0; ks < NT; ++ks) {
+                // 16 keys: two whole blocks when B = 8, else rows 16 ks % B of block 16 ks / B
+                const uint64_t vdesc =
+                    !v_blk ? umma_desc(vb + ks * 16 * 128, kRegion, 1024)
+                    : p.B == 8 ? umma_desc(vb + 2 * ks * blk_bytes, 1024, blk_bytes)
+                               : umma_desc(vb + (16 * ks / p.B) * blk_bytes + (16 * ks % p.B) * 128, p.B * 128, 1024);
+                umma_f16_ta(ocol, pcol + ks * 8, vdesc, idesc_o, (j > 0 || ks > 0));
+                umma_f16_ta(ocol, pcol + kPfKeys / 2 + ks * 8, vdesc, idesc_o, 1u);
+            }
+            umma_commit(pvd0 + 8 * w);
+            if (w == 1) umma_commit(vfree0 + 8 * st(j));
         };
         if (lane == 0) {
-            ok = waited(qbar, 0) && waited(kbar0, 0);
+            ok = waited(qbar, 0) && waited(kfull0, 0);
             tc_fence_after();
-            if (ok) issue_s(0);
-            if (ok && ntiles > 1) {
-                ok = waited(kbar0 + 8, 0);
-                if (ok) issue_s(1);
+            if (ok) {
+                issue_s(0, 0);
+                issue_s(1, 0);
             }
             for (int j = 0; j < ntiles && ok; ++j) {
-                ok = waited(pready, (uint32_t)(j & 1)) && waited(vbar0 + 8 * (j & 1), (uint32_t)((j >> 1) & 1));
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t vb = sV0 + (uint32_t)(j & 1) * kTile;
-#pragma unroll
-                for (int ks = 0; ks < NT; ++ks) {
-                    const uint32_t aoff = (ks >> 2) * kRegion + (ks & 3) * 32;
-                    const uint64_t vdesc = umma_desc(vb + ks * 16 * 128, kRegion, 1024);
-                    umma_f16(tmem + col_o, umma_desc(sPh + aoff, 16, 1024), vdesc, idesc_o, (j > 0 || ks > 0));
-                    umma_f16(tmem + col_o, umma_desc(sPl + aoff, 16, 1024), vdesc, idesc_o, 1u);
-                }
-                umma_commit(pvbar0 + 8 * (j & 1));
-                if (j + 2 < ntiles) {
-                    ok = waited(kbar0 + 8 * (j & 1), (uint32_t)(((j + 2) >> 1) & 1));
-                    if (ok) issue_s(j + 2);  // S[j % 2] was read by softmax j, which signalled p_ready
+                const bool more = j + 1 < ntiles;
+                for (int w = 0; w < 2 && ok; ++w) {
+                    ok = waited(prd0 + 8 * w, (uint32_t)(j & 1)) && (w == 1 || waited(vfull0 + 8 * st(j), ph(j)));
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(w, j);
+                    if (more) {
+                        ok = (w == 1 || waited(kfull0 + 8 * st(j + 1), ph(j + 1))) &&
+                             waited(pvd0 + 8 * w, (uint32_t)(j & 1));
+                        tc_fence_after();
+                        if (ok) issue_s(w, j + 1);
+                    }
                 }
             }
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax warps: thread = query row = TMEM lane
-        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
-        const int r = tid;
-        const int qtok = r / p.G;
+        // ------------------------------------------------------------ softmax: warpgroup w owns query tile w
+        // thread = query row = TMEM lane
+        const int wg = warp >> 2;
+        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t t_s = t_lane + (uint32_t)wg * kPfKeys;
+        const uint32_t t_o = t_lane + 2 * kPfKeys + (uint32_t)wg * D;
+        const int r = tid & (kPfRows - 1);
+        const int qtok = wg * p.TQ + r / p.G;  // query token within the CTA
         const bool row_ok = r < p.TQ * p.G && tok0 + qtok < q_len;
         const int qpos = row_ok ? pos0 + qtok : -1;  // -1 masks every key
-        float m_ref = -INFINITY, l = 0.f;
+        const int first_pos = pos0 + wg * p.TQ;     // position of the tile's first token
         const float NEG_INF = -INFINITY;
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        float m_ref = NEG_INF, l = 0.f;
         for (int j = 0; j < ntiles; ++j) {
             const int k0 = j * kPfKeys;
-            ok = waited(sbar0 + 8 * (j & 1), (uint32_t)((j >> 1) & 1)) && ok;
+            ok = waited(sfull0 + 8 * wg, (uint32_t)(j & 1)) && ok;
             tc_fence_after();
-            const uint32_t t_s = t_lane + (uint32_t)(j & 1) * kPfKeys;
             float v[kPfKeys];
             {
                 uint32_t* u = reinterpret_cast<uint32_t*>(v);
@@ -307,80 +419,85 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                         : "memory");
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
             }
-            // only tiles that reach past the first row's position need the causal mask
-            const bool masked = k0 + kPfKeys - 1 > pos0 || !row_ok;
+            // only tiles that reach past the tile's first position need the causal mask
+            const bool masked = k0 + kPfKeys - 1 > first_pos || !row_ok;
             if (masked) {
 #pragma unroll
                 for (int i = 0; i < kPfKeys; ++i) v[i] = k0 + i <= qpos ? v[i] : NEG_INF;
             }
-            float m_tile = NEG_INF;
+            float mx[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
 #pragma unroll
-            for (int i = 0; i < kPfKeys; ++i) m_tile = fmaxf(m_tile, v[i]);
-            m_tile *= p.scale_log2;
+            for (int i = 0; i < kPfKeys; i += 8) {
+                mx[0] = fmax3(mx[0], v[i], v[i + 1]);
+                mx[1] = fmax3(mx[1], v[i + 2], v[i + 3]);
+                mx[2] = fmax3(mx[2], v[i + 4], v[i + 5]);
+                mx[3] = fmax3(mx[3], v[i + 6], v[i + 7]);
+            }
+            const float m_tile = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * p.scale_log2;
             float m_new = m_ref;
             if (j == 0 || m_tile > m_ref + 8.f) m_new = fmaxf(m_ref, m_tile);
-            const float m_use = m_new == NEG_INF ? 0.f : m_new;
             const float alpha = (j == 0 || m_new == m_ref) ? 1.f : fast_exp2(m_ref - m_new);
-            l *= alpha;
             m_ref = m_new;
-            // P and O are free once PV_{j-1} is done
-            if (j > 0) ok = waited(pvbar0 + 8 * ((j - 1) & 1), (uint32_t)(((j - 1) >> 1) & 1)) && ok;
-            tc_fence_after();
+            const float m_use = m_new == NEG_INF ? 0.f : m_new;
+            const float2 nm2 = make_float2(-m_use, -m_use);
+            // P overwrites S in TMEM: the high parts in the buffer's first 64 columns, the low parts after
+            float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
             for (int c = 0; c < kPfKeys / 32; ++c) {
                 uint32_t hi[16], lo[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    const float p0 = fast_exp2(fmaf(v[32 * c + i], p.scale_log2, -m_use));
-                    const float p1 = fast_exp2(fmaf(v[32 * c + i + 1], p.scale_log2, -m_use));
-                    l += p0 + p1;
-                    hi[i / 2] = Mma<T>::pack(p0, p1);
-                    const float2 f = Mma<T>::unpack(hi[i / 2]);
-                    lo[i / 2] = Mma<T>::pack(p0 - f.x, p1 - f.y);
+                    float2 x = ffma2(make_float2(v[32 * c + i], v[32 * c + i + 1]), sc2, nm2);
+                    x.x = fast_exp2(x.x);
+                    x.y = fast_exp2(x.y);
+                    ls[(i >> 1) & 1] = fadd2(ls[(i >> 1) & 1], x);
+                    hi[i / 2] = Mma<T>::pack(x.x, x.y);
+                    const float2 f = fsub2(x, Mma<T>::unpack(hi[i / 2]));
+                    lo[i / 2] = Mma<T>::pack(f.x, f.y);
                 }
-                const uint32_t row_off = (uint32_t)(c >> 1) * kRegion + (uint32_t)r * 128;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t unit = (uint32_t)((c & 1) * 4 + u) ^ (uint32_t)(r & 7);
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sPh + row_off + unit * 16),
-                                 "r"(hi[4 * u]), "r"(hi[4 * u + 1]), "r"(hi[4 * u + 2]), "r"(hi[4 * u + 3])
-                                 : "memory");
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sPl + row_off + unit * 16),
-                                 "r"(lo[4 * u]), "r"(lo[4 * u + 1]), "r"(lo[4 * u + 2]), "r"(lo[4 * u + 3])
-                                 : "memory");
-                }
+                tmem_st16(t_s + c * 16, hi);
+                tmem_st16(t_s + kPfKeys / 2 + c * 16, lo);
             }
+            const float2 lsum = fadd2(ls[0], ls[1]);
+            l = fmaf(l, alpha, lsum.x + lsum.y);
+            // O_w is rescaled (rarely: only when the maximum grew by more than 2^8) once PV_w(j-1) has landed
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                ok = waited(pvd0 + 8 * wg, (uint32_t)((j - 1) & 1)) && ok;
+                tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     float o[32];
-                    tmem_ld32(t_lane + col_o + c * 32, o);
+                    tmem_ld32(t_o + c * 32, o);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                    tmem_st32(t_lane + col_o + c * 32, o);
+                    tmem_st32(t_o + c * 32, o);
                 }
-                tmem_wait_st();
             }
-            // V rows past the context may hold anything (even NaN): zero them before they meet P = 0
+            // V rows past the context may hold anything (even NaN): tile 0's warpgroup zeroes them before either
+            // query tile's PV (PV_0 is issued first) can meet them with P = 0
             const int nvalid = min(kPfKeys, ctx - k0);
-            if (nvalid < kPfKeys) {
-                ok = waited(vbar0 + 8 * (j & 1), (uint32_t)((j >> 1) & 1)) && ok;
-                const uint32_t vb = sV0 + (uint32_t)(j & 1) * kTile;
-                for (int rr = nvalid + warp; rr < kPfKeys; rr += 4)
+            if (wg == 0 && nvalid < kPfKeys) {
+                ok = waited(vfull0 + 8 * st(j), ph(j)) && ok;
+                const uint32_t vb = sV0 + st(j) * kTile;
+                for (int rr = nvalid + (warp & 3); rr < kPfKeys; rr += 4)
                     for (int dh = 0; dh < DH; ++dh)
                         if (lane < 8)
-                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vb + dh * kRegion +
-                                                                                          rr * 128 + lane * 16),
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
+                                             v_blk ? vb + (uint32_t)(rr / p.B) * blk_bytes +
+                                                         (uint32_t)(dh * p.B + rr % p.B) * 128 + lane * 16
+                                                   : vb + dh * kRegion + rr * 128 + lane * 16),
                                          "r"(0)
                                          : "memory");
             }
+            tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(pready);
+            mbar_arrive(prd0 + 8 * wg);
             if (*abort_flag) break;
         }
         const int jl = ntiles - 1;
-        if (ok) ok = waited(pvbar0 + 8 * (jl & 1), (uint32_t)((jl >> 1) & 1));
+        if (ok) ok = waited(pvd0 + 8 * wg, (uint32_t)(jl & 1));
+        ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             tc_fence_after();
             const float inv = 1.f / l;
@@ -388,7 +505,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 float o[32];
-                tmem_ld32(t_lane + col_o + c * 32, o);
+                tmem_ld32(t_o + c * 32, o);
                 if (row_ok) {
                     if (p.out_dtype == PA_F32) {
                         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow + c * 32);
@@ -410,10 +527,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     if (!ok) {
         if (tid == 0) flag_error(p.err, PA_DEV_ERR_TIMEOUT);
         // let issued tensor-core and copy work land before the memory it uses is released
-        if (tid == 0) {
-            const int jl = ntiles - 1;
-            mbar_wait_bounded(pvbar0 + 8 * (jl & 1), (uint32_t)((jl >> 1) & 1), nullptr, 1000000ull);
-        }
+        if (tid == 0) mbar_wait_bounded(pvd0 + 8, (uint32_t)((ntiles - 1) & 1), nullptr, 1000000ull);
         __syncthreads();
     }
     if (warp == 0) {
@@ -444,11 +558,12 @@ static EncodeTiledFn pf_encode_fn() {
 
 static size_t prefill_smem_bytes(int D) {
     const int DH = D / 64;
-    return 1024 + (size_t)(5 * DH + 4) * kRegion + 96;  // Q, K[2], V[2], P_hi, P_lo, barriers
+    return 1024 + (size_t)(2 + 2 * kPfStages) * DH * kRegion + 256;  // Q[2], K[NS], V[NS], barriers
 }
 
 template <typename T, int D>
-static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tkv) {
+static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tkv,
+                             const CUtensorMap& tkv_blk) {
     auto kern = prefill_kernel<T, D>;
     const size_t smem = prefill_smem_bytes(D);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -470,8 +585,8 @@ static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const 
     p.out_dtype = a.out_dtype;
     p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
     p.err = a.dev_err;
-    const dim3 grid((a.max_q_len + p.TQ - 1) / p.TQ, a.H_kv, a.N);
-    e = launch_kernel(kern, grid, dim3(kPfThreads), smem, a.stream, tq, tkv, p);
+    const dim3 grid((a.max_q_len + 2 * p.TQ - 1) / (2 * p.TQ), a.H_kv, a.N);
+    e = launch_kernel(kern, grid, dim3(kPfThreads), smem, a.stream, tq, tkv, tkv_blk, p);
     count_launch();
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "prefill launch");
 }
@@ -500,9 +615,17 @@ pa_status launch_prefill(const PrefillArgs& a) {
     r = fn(&tkv, dt, 5, const_cast<void*>(a.pool), pd, ps, pb, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(pool) failed (CUresult %d)", (int)r);
+    // the same view, box = one whole block (both column halves)
+    CUtensorMap tkv_blk;
+    std::memset(&tkv_blk, 0, sizeof tkv_blk);
+    pb[2] = (cuuint32_t)DH;
+    r = fn(&tkv_blk, dt, 5, const_cast<void*>(a.pool), pd, ps, pb, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(pool blocks) failed (CUresult %d)", (int)r);
     if (a.kv_dtype == PA_BF16)
-        return a.D == 128 ? run_prefill<__nv_bfloat16, 128>(a, tq, tkv) : run_prefill<__nv_bfloat16, 64>(a, tq, tkv);
-    return a.D == 128 ? run_prefill<__half, 128>(a, tq, tkv) : run_prefill<__half, 64>(a, tq, tkv);
+        return a.D == 128 ? run_prefill<__nv_bfloat16, 128>(a, tq, tkv, tkv_blk)
+                          : run_prefill<__nv_bfloat16, 64>(a, tq, tkv, tkv_blk);
+    return a.D == 128 ? run_prefill<__half, 128>(a, tq, tkv, tkv_blk) : run_prefill<__half, 64>(a, tq, tkv, tkv_blk);
 }
 
 }  // namespace pa
