@@ -190,7 +190,8 @@ pa_status pa_decode_contiguous(void* out, pa_dtype out_dtype, const void* q, con
  * Runs on the tensor cores (tcgen05, accumulators in TMEM).  A chunk longer
  * than its context is flagged PA_DEV_ERR_CTX and not computed.
  * Supported: kv_dtype F16/BF16, D in {64, 128}, B in {8, 16, 32},
- * H_q / H_kv <= 128, N <= 65535, scale > 0.
+ * H_q / H_kv <= 128, N <= 65535, scale > 0.  out, q and pool must be
+ * 16-byte aligned, an fp32 out 32-byte aligned (PA_ERR_INVALID otherwise).
  * ---------------------------------------------------------------------- */
 pa_status pa_prefill(void* out, pa_dtype out_dtype, const void* q, const void* pool, const int32_t* block_tables,
                      const int32_t* ctx_lens, const int32_t* q_start, int N, int T, int H_q, int H_kv, int D, int B,

@@ -263,6 +263,8 @@ pa_status pa_prefill(void* out, pa_dtype out_dtype, const void* q, const void* p
     if (T == 0 || max_q_len == 0) return PA_OK;
     if (!out || !q || !pool || !block_tables || !ctx_lens || !q_start) return fail(PA_ERR_INVALID, "null pointer");
     if (!aligned16(out) || !aligned16(q) || !aligned16(pool)) return fail(PA_ERR_INVALID, "16-byte alignment");
+    if (out_dtype == PA_F32 && (reinterpret_cast<uintptr_t>(out) & 31u))
+        return fail(PA_ERR_INVALID, "an fp32 out must be 32-byte aligned");
     PrefillArgs a;
     a.out = out;
     a.out_dtype = out_dtype;

@@ -508,11 +508,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                 tmem_ld32(t_o + c * 32, o);
                 if (row_ok) {
                     if (p.out_dtype == PA_F32) {
-                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow + c * 32);
+                        // 256-bit stores: each lane writes whole 32-byte sectors of its row (the host checks
+                        // that `out` is 32-byte aligned; rows are D floats long)
+                        float* dst = static_cast<float*>(p.out) + orow + c * 32;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
-                                                 o[4 * i + 3] * inv);
+                        for (int i = 0; i < 4; ++i)
+                            asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 8 * i),
+                                         "f"(o[8 * i] * inv), "f"(o[8 * i + 1] * inv), "f"(o[8 * i + 2] * inv),
+                                         "f"(o[8 * i + 3] * inv), "f"(o[8 * i + 4] * inv), "f"(o[8 * i + 5] * inv),
+                                         "f"(o[8 * i + 6] * inv), "f"(o[8 * i + 7] * inv)
+                                         : "memory");
                     } else {
                         T* dst = static_cast<T*>(p.out) + orow + c * 32;
 #pragma unroll

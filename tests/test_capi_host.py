@@ -47,6 +47,16 @@ def test_device_calls_reject_bad_arguments_before_touching_the_gpu():
     assert st == pa.PA_ERR_UNSUPPORTED and "out_dtype" in pa.last_error()
     st = L.pa_partition_reduce(None, 2, None, None, None, None, 0, 4, 128, None, None)
     assert st == pa.PA_OK
+    # pa_prefill: placeholder addresses are never dereferenced because validation fails first
+    out, q, pool, tab, ctx, qs = 0x1010, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000
+
+    def prefill(out=out, out_dtype=2, B=16, scale=0.1):
+        return L.pa_prefill(out, out_dtype, q, pool, tab, ctx, qs, 1, 1, 8, 8, 128, B, 1, 1, 1, scale, 1, None, None)
+
+    assert prefill() == pa.PA_ERR_INVALID and "32-byte" in pa.last_error()
+    assert prefill(out=0x1008, out_dtype=1) == pa.PA_ERR_INVALID and "16-byte" in pa.last_error()
+    assert prefill(out=0x1020, B=4) == pa.PA_ERR_UNSUPPORTED
+    assert prefill(out=0x1020, scale=0.0) == pa.PA_ERR_INVALID
 
 
 def _run_same_ops(NB, B, order, ops):
