@@ -418,12 +418,14 @@ def run_ours(args):
 
 
 def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world, tab):
-    """Decode steps through the public API from pinned host buffers.  Inside the timed region, per step:
-    host block allocation (slots + block-table updates), one host->device copy of the step's inputs
-    (q, new K/V, slots, lengths, table updates), the table update, cache write and decode kernels, and the
-    device->host copy of the output, then a synchronisation.  The allocation of step i+1 depends only on the
-    sequence lengths, so the host runs it while the device executes step i (before that step's sync); the
-    allocation of the first timed step is the warm-up's last overlap."""
+    """Decode steps through the public API from pinned host buffers.  Each step's inputs (q and the new K/V) sit in
+    a pinned staging buffer of their own; the host block allocation of the step (slots, lengths and block-table
+    updates, padded to a fixed count with skipped rows) is written into the same buffer.  Inside the timed region,
+    per step: the host allocation of the NEXT step (it needs only the lengths, so it runs while the device works)
+    and one CUDA graph launch that copies the staging buffer host->device, applies the table updates, writes the
+    cache, runs the decode (plan, attention, merge) and copies the output device->host; then a synchronisation.
+    The graphs hold the same library calls a user would make eagerly, captured once per staging buffer before
+    the timed region: they remove the host launch latency, not device work."""
     import torch
 
     import paged_kv_cache_302_gb300 as pa
@@ -434,18 +436,19 @@ def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world, tab
     seq_ids = list(range(w.N))
     ones = np.ones(w.N, dtype=np.int32)
     ctx = np.array([alloc.seq_len(s) for s in seq_ids], dtype=np.int32)
+    cap_u = 2 * w.N + 1   # table updates per step: at most a new block and a copy-on-write replacement per sequence
 
     def al(x):
         return (x + 15) // 16 * 16
 
-    # staging layout (bytes): q | k | v | slots int64 | ctx int32 | table updates int32[.,3]
+    # staging layout (bytes): q | k | v | slots int64 | ctx int32 | table updates int32[cap_u, 3]
     nq, nk = w.N * w.H_q * w.D * 2, w.N * w.H_kv * w.D * 2
     o_k = al(nq)
     o_v = o_k + al(nk)
     o_s = o_v + al(nk)
     o_c = o_s + al(w.N * 8)
     o_u = o_c + al(w.N * 4)
-    total = o_u + al(2 * w.N * 12)
+    total = o_u + al(cap_u * 12)
     stage = []
     for q, k, v in W.decode_steps(w, nsteps):
         h = torch.empty(total, dtype=torch.uint8).pin_memory()
@@ -460,10 +463,22 @@ def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world, tab
     d_v = d_stage[o_v:o_v + nk].view(torch.bfloat16).view(w.N, w.H_kv, w.D)
     d_slot = d_stage[o_s:o_s + w.N * 8].view(torch.int64)
     d_ctx = d_stage[o_c:o_c + w.N * 4].view(torch.int32)
+    d_upd = d_stage[o_u:o_u + cap_u * 12].view(torch.int32).view(cap_u, 3)
     h_out = torch.empty((w.N, w.H_q, w.D), dtype=torch.float32).pin_memory()
     d2h = h_out.numel() * 4
-    h2d_bytes = []
     e2e_bytes = []
+
+    graphs = []
+    for i in range(nsteps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            d_stage.copy_(stage[i], non_blocking=True)
+            pa.pa_update_block_tables(tab, d_upd, dev_err=err)
+            pa.pa_reshape_and_cache(d_k, d_v, pool, d_slot, dev_err=err)
+            pa.pa_decode(out, d_q, pool, tab, d_ctx, max_ctx, partition_tokens=pt, workspace=ws, dev_err=err)
+            h_out.copy_(out, non_blocking=True)
+        graphs.append(g)
+    torch.cuda.synchronize()
 
     def prepare(i):
         """Host block allocation of step i into its staging buffer (it needs the lengths only)."""
@@ -473,25 +488,19 @@ def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world, tab
         hb = stage[i].numpy()
         hb[o_s:o_s + w.N * 8] = sl.view(np.uint8)
         hb[o_c:o_c + w.N * 4] = ctx.view(np.uint8)
-        nu = upd.shape[0]
-        hb[o_u:o_u + nu * 12] = np.ascontiguousarray(upd).view(np.uint8).reshape(-1)
-        return nu, pairs, int(ctx.astype(np.int64).sum()) * per_tok
+        u = np.full((cap_u, 3), -1, dtype=np.int32)
+        u[:upd.shape[0]] = upd
+        hb[o_u:o_u + cap_u * 12] = u.view(np.uint8).reshape(-1)
+        return pairs, int(ctx.astype(np.int64).sum()) * per_tok
 
     def e2e_step(i, prep, next_i):
         """Runs step i; the host prepares step next_i while the device works."""
-        nu, pairs, nbytes = prep
-        used = o_u + nu * 12
-        d_stage[:used].copy_(stage[i][:used], non_blocking=True)
-        if nu:
-            pa.pa_update_block_tables(tab, d_stage[o_u:o_u + nu * 12].view(torch.int32).view(nu, 3), dev_err=err)
-        if pairs.size:
+        pairs, nbytes = prep
+        if pairs.size:   # copy-on-write before the step's cache write (none in this workload: no forks)
             pa.pa_copy_blocks(pool, torch.from_numpy(pairs).to(dev), dev_err=err)
-        pa.pa_reshape_and_cache(d_k, d_v, pool, d_slot, dev_err=err)
-        pa.pa_decode(out, d_q, pool, tab, d_ctx, max_ctx, partition_tokens=pt, workspace=ws, dev_err=err)
-        h_out.copy_(out, non_blocking=True)
+        graphs[i].replay()
         nxt = prepare(next_i) if next_i is not None else None
         torch.cuda.current_stream().synchronize()
-        h2d_bytes.append(used)
         return nbytes, nxt
 
     prep = prepare(0)
@@ -499,7 +508,6 @@ def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world, tab
         _, prep = e2e_step(i, prep, i + 1)
     if world > 1:
         torch.distributed.barrier()
-    h2d_bytes.clear()
     t0 = time.perf_counter()
     for i in range(args.warmup, nsteps):
         nbytes, prep = e2e_step(i, prep, i + 1 if i + 1 < nsteps else None)
@@ -508,7 +516,7 @@ def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world, tab
     assert int(err.item()) == 0, f"device error flags {int(err.item())}"
     t_e2e, e2e_total = whole_job(t_e2e, sum(e2e_bytes), dev)
     e2e_value = e2e_total / t_e2e / 1e9
-    return e2e_value, int(round(sum(h2d_bytes) / len(h2d_bytes))), d2h
+    return e2e_value, total, d2h
 
 
 def run_swap(args):

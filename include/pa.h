@@ -118,10 +118,11 @@ pa_status pa_swap_blocks(void* dst_pool, int NB_dst, const void* src_pool, int N
  * the device and only changed entries travel).
  * tables: [N][MB] int32 device memory; updates: [n][3] int32 device memory
  * (row, logical block, physical block), as pa_alloc_append_batch emits them.
- * Sets tables[row][logical block] = physical block.  Entries with row outside
- * [0, N) or logical block outside [0, MB) are skipped and flagged
- * PA_DEV_ERR_BLOCK.  Two updates of the same entry race (the allocator never
- * emits that).  n == 0 is a no-op.
+ * Sets tables[row][logical block] = physical block.  An entry with a negative
+ * row is padding and is skipped (so a fixed-size update list can be captured
+ * in a CUDA graph); entries with row >= N or logical block outside [0, MB)
+ * are skipped and flagged PA_DEV_ERR_BLOCK.  Two updates of the same entry
+ * race (the allocator never emits that).  n == 0 is a no-op.
  * ---------------------------------------------------------------------- */
 pa_status pa_update_block_tables(int32_t* tables, int N, int MB, const int32_t* updates, int n, int* dev_err,
                                  void* stream);

@@ -106,7 +106,7 @@ pa_status launch_copy_blocks(void* pool, const int64_t* pairs, int n, int NB, in
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "copy_blocks launch");
 }
 
-// One thread per table update (row, logical block, physical block).
+// One thread per table update (row, logical block, physical block); a negative row is padding.
 __global__ void __launch_bounds__(256) update_tables_kernel(int32_t* __restrict__ tables, int N, int MB,
                                                             const int3* __restrict__ upd, int n, int* err) {
     griddep_wait();
@@ -114,7 +114,8 @@ __global__ void __launch_bounds__(256) update_tables_kernel(int32_t* __restrict_
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     const int3 u = upd[i];
-    if (u.x < 0 || u.x >= N || u.y < 0 || u.y >= MB) {
+    if (u.x < 0) return;
+    if (u.x >= N || u.y < 0 || u.y >= MB) {
         flag_error(err, PA_DEV_ERR_BLOCK);
         return;
     }

@@ -89,6 +89,10 @@ def test_table_updates_keep_the_device_tables_current():
         want, _ = a.block_tables(order, MB)
         torch.cuda.synchronize()
         assert np.array_equal(dev.cpu().numpy(), want) and err.item() == 0
+    pad = torch.tensor([[-1, 0, 1], [-7, MB + 3, 2]], dtype=torch.int32, device="cuda")  # padding rows
+    pa.pa_update_block_tables(dev, pad, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0 and np.array_equal(dev.cpu().numpy(), want)
     bad = torch.tensor([[w.N, 0, 1], [0, MB, 1]], dtype=torch.int32, device="cuda")
     pa.pa_update_block_tables(dev, bad, dev_err=err)
     torch.cuda.synchronize()
