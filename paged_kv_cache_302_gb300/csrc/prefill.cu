@@ -325,15 +325,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         // ------------------------------------------------------------ MMA issuer
         // S_w(j) = Q_w K_j^T goes to TMEM buffer w and is overwritten there by P_w(j); O_w += P_w(j) V_j.
         // S_w(j+1) reuses the buffer once PV_w(j) has read P_w(j).
+        // Descriptors are built once per operand and advanced per k-step by adding the byte offset / 16 to their
+        // 14-bit address field (shared-memory addresses stay below 256 KB, so the field never carries); building
+        // both 64-bit descriptors per instruction slowed the single issuing thread (measured 789 -> 824 TFLOP/s).
+        const uint64_t dq0 = umma_desc(sQ0, 16, 1024), dq1 = umma_desc(sQ0 + kTile, 16, 1024);
         auto issue_s = [&](int w, int j) {
             const uint32_t kb = sK0 + st(j) * kTile;
-            const uint32_t qb = sQ0 + w * kTile;
+            const uint64_t dq = w ? dq1 : dq0;
+            const uint64_t dk = k_blk ? umma_desc(kb, 16, blk_bytes) : umma_desc(kb, 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < NK; ++ks) {
-                const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
-                const uint64_t kdesc = k_blk ? umma_desc(kb + (ks >> 2) * 1024 + (ks & 3) * 32, 16, blk_bytes)
-                                             : umma_desc(kb + off, 16, 1024);
-                umma_f16(tmem + (uint32_t)w * kPfKeys, umma_desc(qb + off, 16, 1024), kdesc, idesc_s, ks > 0);
+                constexpr uint32_t kR16 = kRegion >> 4;
+                const uint32_t qoff = (ks >> 2) * kR16 + (ks & 3) * 2;
+                const uint32_t koff = k_blk ? (ks >> 2) * 64 + (ks & 3) * 2 : qoff;
+                umma_f16(tmem + (uint32_t)w * kPfKeys, dq + qoff, dk + koff, idesc_s, ks > 0);
             }
             umma_commit(sfull0 + 8 * w);
             if (w == 1) umma_commit(kfree0 + 8 * st(j));  // K_j has served both query tiles
@@ -342,13 +347,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             const uint32_t vb = sV0 + st(j) * kTile;
             const uint32_t pcol = tmem + (uint32_t)w * kPfKeys;
             const uint32_t ocol = tmem + 2 * kPfKeys + (uint32_t)w * D;
+            const uint64_t dv = !v_blk ? umma_desc(vb, kRegion, 1024) : umma_desc(vb, 1024, blk_bytes);
+            const uint32_t vstep = !v_blk ? (16 * 128) >> 4 : (2 * blk_bytes) >> 4;
 #pragma unroll
             for (int ks = 0; ks < NT; ++ks) {
-                // 16 keys: two whole blocks when B = 8, else rows 16 ks % B of block 16 ks / B
-                const uint64_t vdesc =
-                    !v_blk ? umma_desc(vb + ks * 16 * 128, kRegion, 1024)
-                    : p.B == 8 ? umma_desc(vb + 2 * ks * blk_bytes, 1024, blk_bytes)
-                               : umma_desc(vb + (16 * ks / p.B) * blk_bytes + (16 * ks % p.B) * 128, p.B * 128, 1024);
+                const uint64_t vdesc = dv + (uint64_t)(ks * vstep);
                 umma_f16_ta(ocol, pcol + ks * 8, vdesc, idesc_o, (j > 0 || ks > 0));
                 umma_f16_ta(ocol, pcol + kPfKeys / 2 + ks * 8, vdesc, idesc_o, 1u);
             }
