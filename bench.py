@@ -609,22 +609,27 @@ def run_prefill(args):
 
 
 def _time_decode(fn, att_ev, reps=20, warm=3):
-    """Median event time of a decode call and of its attention kernel (seconds)."""
+    """(whole call, attention kernel) in seconds.  The whole call is timed over `reps` back-to-back calls
+    between two events (the host enqueues ahead, as in a decode loop); the attention kernel is the median of
+    per-call events around it, taken in a second pass (those events stop the schedule/attention overlap)."""
     import torch
 
     for _ in range(warm):
         fn(None)
     torch.cuda.synchronize()
-    ts, ta = [], []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
     for _ in range(reps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
+        fn(None)
+    e1.record()
+    torch.cuda.synchronize()
+    t_call = e0.elapsed_time(e1) * 1e-3 / reps
+    ta = []
+    for _ in range(reps):
         fn(att_ev)
-        e1.record()
         torch.cuda.synchronize()
-        ts.append(e0.elapsed_time(e1) * 1e-3)
         ta.append(att_ev[0].elapsed_time(att_ev[1]) * 1e-3)
-    return float(np.median(ts)), float(np.median(ta))
+    return t_call, float(np.median(ta))
 
 
 def run_configs(args):

@@ -50,11 +50,22 @@ struct __align__(16) StageMeta {
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Partition length for partition_tokens == 0: kDefaultPartition unless PA_DECODE_PARTITION names another
+// multiple of the stage length (read once; a tuning knob like PA_DECODE_CTAS_PER_SM).
+static int default_partition() {
+    static const int pt = [] {
+        const char* v = std::getenv("PA_DECODE_PARTITION");
+        const int x = (v && *v) ? std::atoi(v) : 0;
+        return x > 0 && x % kStageTok == 0 ? x : kDefaultPartition;
+    }();
+    return pt;
+}
+
 bool workspace_layout(int N, int H_q, int H_kv, int D, int max_ctx, int partition_tokens, WorkspaceLayout* L) {
     if (N <= 0 || H_q <= 0 || H_kv <= 0 || D <= 0 || max_ctx <= 0) return false;
     int PT;
     if (partition_tokens == 0)
-        PT = kDefaultPartition;
+        PT = default_partition();
     else if (partition_tokens == -1)
         PT = kUnpartitioned;
     else if (partition_tokens > 0 && partition_tokens % kStageTok == 0)
