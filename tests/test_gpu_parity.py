@@ -152,6 +152,33 @@ def test_ragged_lengths_cover_every_tail():
         C.assert_close(out, ref, f"ragged pt={pt}")
 
 
+def test_single_token_contexts_return_that_token_value_row():
+    """Degenerate case: with ctx = 1 the softmax weight is 1, so every head returns V_0 (to within the fp32
+    rounding of the base-2 exponent of a product's residual: a relative 4e-7)."""
+    N, NB = 300, 400
+    w = W.Workload("ctx1", 21, N, 32, 8, 128, 16, "bf16", np.ones(N, np.int32), NB,
+                   np.random.default_rng(21).permutation(NB).astype(np.int32))
+    c = C.build_paged(w)
+    out = C.gpu_decode(c).cpu().numpy()
+    v0 = W.bits_to_float(c.host_pool[c.tables[:, 0], 0, 1], w.dtype)          # [N, H_kv, D]
+    want = np.repeat(v0, w.G, axis=1).astype(np.float32)                         # head h reads KV head h // G
+    np.testing.assert_allclose(out, want, rtol=4e-7, atol=0)
+
+
+def test_many_short_sequences_every_output():
+    """5000 sequences of 1..40 tokens: the schedule handles several sequences per thread, most work items are
+    single ragged partitions, and every output is checked."""
+    rng = np.random.default_rng(22)
+    N, B = 5000, 16
+    ctx = rng.integers(1, 41, size=N).astype(np.int32)
+    NB = int(((ctx + B - 1) // B).sum()) + 16
+    w = W.Workload("many", 22, N, 8, 2, 64, B, "f16", ctx, NB, rng.permutation(NB).astype(np.int32))
+    c = C.build_paged(w)
+    ref = C.oracle_decode(c)
+    for pt in (0, 32):
+        C.assert_close(C.gpu_decode(c, partition_tokens=pt).cpu().numpy(), ref, f"many short pt={pt}")
+
+
 def test_block_relabelling_gives_identical_bits():
     w = W.llama3_8b(n_seqs=12)
     c = C.build_paged(w, check_pool=False)
@@ -210,9 +237,10 @@ def test_low_precision_output_is_the_rounded_fp32_output():
         assert np.all(np.abs(W.bits_to_float(bits, "bf16") - ref) <= C.ATOL + half_ulp)
 
 
-def test_partition_reduce_standalone_matches_oracle_merge():
-    rng = np.random.default_rng(4)
-    R, P, D = 37, 9, 128
+@pytest.mark.parametrize("R,P,D", [(37, 9, 128), (37, 40, 128), (11, 300, 128), (23, 33, 64)])
+def test_partition_reduce_standalone_matches_oracle_merge(R, P, D):
+    """Warp-per-row merge (P < 32) and CTA-per-row merge (P >= 32, rows of up to 300 partitions)."""
+    rng = np.random.default_rng(4 + P)
     m2 = (rng.normal(size=(R, P)) * 3).astype(np.float32)
     l = rng.uniform(0.5, 40.0, size=(R, P)).astype(np.float32)
     acc = rng.normal(size=(R, P, D)).astype(np.float32)
