@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -102,12 +103,31 @@ def config_dict(w: W.Workload, pt: int) -> dict:
 
 # ----------------------------------------------------------------------------- oracle timing
 
-def oracle_sample_rate(w: W.Workload, host_pool, tables, ctx, q, target_s: float):
-    """Time the oracle over whole sequences (every query head) until ~target_s of CPU work."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the architecture)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.machine()
+
+
+def oracle_sample_rate(w: W.Workload, host_pool, tables, ctx, q, target_s: float, nthreads: int = 0):
+    """Time the oracle over whole sequences (every query head) until ~target_s of CPU work
+    (nthreads 0: every host core)."""
     import oracle
 
     order = np.random.default_rng(9).permutation(w.N)
-    nthreads = oracle.num_threads()
+    nthreads = nthreads or oracle.num_threads()
     done_bytes, t_total, seqs = 0, 0.0, 0
     per_tok = 2 * w.H_kv * w.D * w.elem_bytes
     for chunk in np.array_split(order, 16):
@@ -389,10 +409,14 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host_pool, tables_h, ctx_h, _ = host_state(w)
-        rate, cores, seqs, secs = oracle_sample_rate(w, host_pool, tables_h, ctx_h, W.queries(w), args.cpu_seconds)
+        qh = W.queries(w)
+        rate, cores, seqs, secs = oracle_sample_rate(w, host_pool, tables_h, ctx_h, qh, args.cpu_seconds)
+        rate1, _, seqs1, secs1 = oracle_sample_rate(w, host_pool, tables_h, ctx_h, qh, min(args.cpu_seconds, 3.0), 1)
         cpu = {"value": rate, "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"fp64 oracle, all {w.H_q} query heads of {seqs} of the {w.N} sequences "
-                         f"(first decode step's contexts), {secs:.1f} s wall"}
+                         f"(first decode step's contexts), {secs:.1f} s wall",
+               "single_thread_value": rate1,
+               "single_thread_sample": f"{seqs1} sequences, {secs1:.1f} s", "cpu_model": cpu_model()}
 
     if rank == 0:
         line = {
