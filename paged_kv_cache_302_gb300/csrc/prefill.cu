@@ -6,21 +6,23 @@
 // the block table.  Each query row follows the decode equation with its
 // context cut at its own position.
 //
-// One CTA (4 warps) owns a tile of 128 query rows: 128/G query tokens times the
-// G query heads of one KV head, so every K/V byte a tile loads serves G heads.
-// Per 128-key tile:
-//   * TMA lands the tile's K and V rows (one box per KV block and 64-column
-//     half, 128-byte swizzled) through the block table;
-//   * one thread issues S = Q K^T as tcgen05.mma (M 128, N 128, K 16 steps)
-//     into TMEM columns [0, 128);
-//   * every thread owns one TMEM lane = one query row: it reads its S row with
-//     tcgen05.ld, masks causally, keeps the running maximum (rescaling the
-//     output only when the maximum grows by more than 2^8), and writes the
-//     probabilities to shared memory as a high and a low 16-bit part;
-//   * one thread issues O += P_hi V + P_lo V (V is an MN-major operand) into
-//     TMEM columns [128, 128 + D).
-// Finally every thread reads its O row, divides by its exponential sum and
-// stores the row.
+// A query tile is 128 rows: 128/G query tokens times the G query heads of one
+// KV head, so every K/V byte loaded serves G heads.  A CTA owns two consecutive
+// query tiles, which share every K/V tile it loads (320 threads):
+//   * warp 8 (TMA): both Q tiles once, then K and V of each 128-key tile into a
+//     two-stage ring, through the block table, 128-byte swizzled; lane b issues
+//     the copies of the tile's b-th KV block;
+//   * warp 9 (MMA, one thread): S_w = Q_w K^T as tcgen05.mma (M 128, N 128,
+//     K 16 steps) into TMEM columns [128w, 128w + 128), and O_w += P_hi V +
+//     P_lo V with P read from those same TMEM columns (the A operand) and V an
+//     MN-major shared-memory operand; O_w sits in TMEM columns 256 + D w;
+//   * warps 0-3 and 4-7 (softmax, one warpgroup per query tile): every thread
+//     owns one TMEM lane = one query row; it reads its S row with tcgen05.ld,
+//     masks causally, keeps the running maximum (rescaling O only when the
+//     maximum grows by more than 2^8), and writes the probabilities back over S
+//     as a high and a low 16-bit part (tcgen05.st).
+// Hand-offs are mbarriers; every wait is bounded.  Finally every thread reads
+// its O row, divides by its exponential sum and stores the row.
 #include <cuda.h>
 
 #include <algorithm>
