@@ -8,10 +8,11 @@
 // リクエスト単位のKVキャッシュインデキシング (request r at offset r * S).
 //
 // Three kernels per call:
-//  1. plan_kernel (1 CTA): splits every context into partitions of PT tokens
-//     and writes one work record (seq, kv head, partition, ctx) per
-//     (partition, kv head) in longest-first order: whole partitions in sequence
-//     order, then the ragged last partitions by decreasing length.
+//  1. plan_kernel (1 CTA; plan_coop_kernel up to 128 sequences): splits every
+//     context into partitions of PT tokens and writes one work record (seq, kv
+//     head, partition, ctx) per (partition, kv head) in longest-first order:
+//     whole partitions in sequence order, then the ragged last partitions by
+//     decreasing length.
 //  2. attend_kernel (persistent, 4 CTAs per SM, 2 warps each): CTA c takes
 //     records c, c + grid, ...  Warp 1 (producer) streams each record's K/V
 //     through a ring of shared-memory stages with TMA: one 5-D tensor copy per
@@ -21,7 +22,9 @@
 //     mma.sync m16n8k16 (tokens on M, the <= 8 query heads of the KV head on N),
 //     an online softmax in base 2 between stages, and writes the normalised
 //     output, or the partition's (m2, l, acc) when the context has several.
-//  3. partition_reduce_kernel: merges the partials of multi-partition rows.
+//  3. partition_reduce_kernel (one warp per row; partition_reduce_wide_kernel,
+//     one CTA per row, from 32 partitions per row): merges the partials of
+//     multi-partition rows.
 // Each kernel is launched with programmatic stream serialisation, so its CTAs
 // start while the previous kernel drains and wait (griddepcontrol.wait)
 // before touching memory.
