@@ -223,7 +223,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = blockIdx.z, g = blockIdx.y;
     const int qs = p.q_start[s], q_len = p.q_start[s + 1] - qs;
-    const int tok0 = blockIdx.x * 2 * p.TQ;  // first query token of tile 0; tile 1 follows at tok0 + TQ
+    // query-tile pairs are dispatched latest first: under the causal mask they have the most keys, so the last
+    // CTAs to run are the shortest
+    const int tok0 = (gridDim.x - 1 - blockIdx.x) * 2 * p.TQ;  // first query token of tile 0; tile 1 at tok0 + TQ
     if (tok0 >= q_len) return;  // uniform per CTA, before any allocation
     const int ctx = p.ctx_lens[s];
     if (q_len > ctx || ctx > p.MB * p.B || q_len < 0) {
