@@ -5,6 +5,8 @@
 #include <cstdlib>
 #include <cstring>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "pa_internal.h"
 
 namespace pa {
@@ -25,6 +27,26 @@ pa_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+// NVTX ranges around every device call, for profiler timelines; off unless PA_NVTX is set to a non-zero value
+// (read once), so a call costs one predictable branch when they are off.
+static bool nvtx_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("PA_NVTX");
+        return v && *v && *v != '0';
+    }();
+    return on;
+}
+
+struct NvtxRange {
+    bool on;
+    explicit NvtxRange(const char* name) : on(nvtx_enabled()) {
+        if (on) nvtxRangePushA(name);
+    }
+    ~NvtxRange() {
+        if (on) nvtxRangePop();
+    }
+};
 
 bool pdl_enabled() {
     static const bool on = [] {
@@ -73,6 +95,7 @@ uint64_t pa_launch_count(void) { return g_launches.load(std::memory_order_relaxe
 
 pa_status pa_reshape_and_cache(const void* k, const void* v, void* pool, const int64_t* slot_mapping, int T, int NB,
                                int B, int H_kv, int D, pa_dtype dtype, int* dev_err, void* stream) {
+    const NvtxRange nvtx_range("pa_reshape_and_cache");
     g_msg[0] = 0;
     if (!kv_dtype_ok(dtype)) return fail(PA_ERR_UNSUPPORTED, "dtype must be F16 or BF16");
     if (T < 0 || NB <= 0 || B <= 0 || H_kv <= 0 || D <= 0) return fail(PA_ERR_INVALID, "bad sizes");
@@ -88,6 +111,7 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* pool, const i
 
 pa_status pa_copy_blocks(void* pool, const int64_t* pairs, int n, int NB, int B, int H_kv, int D, pa_dtype dtype,
                          int* dev_err, void* stream) {
+    const NvtxRange nvtx_range("pa_copy_blocks");
     g_msg[0] = 0;
     if (!kv_dtype_ok(dtype)) return fail(PA_ERR_UNSUPPORTED, "dtype must be F16 or BF16");
     if (n < 0 || NB <= 0 || B <= 0 || H_kv <= 0 || D <= 0) return fail(PA_ERR_INVALID, "bad sizes");
@@ -113,6 +137,7 @@ static pa_status check_device_accessible(const void* p, const char* what) {
 
 pa_status pa_swap_blocks(void* dst_pool, int NB_dst, const void* src_pool, int NB_src, const int64_t* pairs, int n,
                          int B, int H_kv, int D, pa_dtype dtype, int* dev_err, void* stream) {
+    const NvtxRange nvtx_range("pa_swap_blocks");
     g_msg[0] = 0;
     if (!kv_dtype_ok(dtype)) return fail(PA_ERR_UNSUPPORTED, "dtype must be F16 or BF16");
     if (n < 0 || NB_dst <= 0 || NB_src <= 0 || B <= 0 || H_kv <= 0 || D <= 0) return fail(PA_ERR_INVALID, "bad sizes");
@@ -133,6 +158,7 @@ pa_status pa_swap_blocks(void* dst_pool, int NB_dst, const void* src_pool, int N
 pa_status pa_write_contiguous(const void* k, const void* v, void* k_buf, void* v_buf, const int32_t* req_ids,
                               const int32_t* positions, int T, int N_max, int S_max, int H_kv, int D, pa_dtype dtype,
                               int* dev_err, void* stream) {
+    const NvtxRange nvtx_range("pa_write_contiguous");
     g_msg[0] = 0;
     if (!kv_dtype_ok(dtype)) return fail(PA_ERR_UNSUPPORTED, "dtype must be F16 or BF16");
     if (T < 0 || N_max <= 0 || S_max <= 0 || H_kv <= 0 || D <= 0) return fail(PA_ERR_INVALID, "bad sizes");
@@ -147,6 +173,7 @@ pa_status pa_write_contiguous(const void* k, const void* v, void* k_buf, void* v
 
 pa_status pa_update_block_tables(int32_t* tables, int N, int MB, const int32_t* updates, int n, int* dev_err,
                                  void* stream) {
+    const NvtxRange nvtx_range("pa_update_block_tables");
     g_msg[0] = 0;
     if (N <= 0 || MB <= 0 || n < 0) return fail(PA_ERR_INVALID, "bad sizes");
     if (n == 0) return PA_OK;
@@ -166,6 +193,7 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* po
                     const int32_t* ctx_lens, int N, int H_q, int H_kv, int D, int B, int MB, int NB, int max_ctx,
                     float scale, int partition_tokens, void* workspace, size_t ws_bytes, pa_dtype kv_dtype,
                     int* dev_err, void* const* attend_events, void* stream) {
+    const NvtxRange nvtx_range("pa_decode");
     g_msg[0] = 0;
     pa_status st = check_decode_common(out_dtype, kv_dtype, out, q, ctx_lens, N, H_q, H_kv, D, max_ctx,
                                        partition_tokens, workspace, ws_bytes);
@@ -208,6 +236,7 @@ pa_status pa_decode_contiguous(void* out, pa_dtype out_dtype, const void* q, con
                                int N_max, int S_max, int max_ctx, float scale, int partition_tokens, void* workspace,
                                size_t ws_bytes, pa_dtype kv_dtype, int* dev_err, void* const* attend_events,
                                void* stream) {
+    const NvtxRange nvtx_range("pa_decode_contiguous");
     g_msg[0] = 0;
     pa_status st = check_decode_common(out_dtype, kv_dtype, out, q, ctx_lens, N, H_q, H_kv, D, max_ctx,
                                        partition_tokens, workspace, ws_bytes);
@@ -247,6 +276,7 @@ pa_status pa_decode_contiguous(void* out, pa_dtype out_dtype, const void* q, con
 pa_status pa_prefill(void* out, pa_dtype out_dtype, const void* q, const void* pool, const int32_t* block_tables,
                      const int32_t* ctx_lens, const int32_t* q_start, int N, int T, int H_q, int H_kv, int D, int B,
                      int MB, int NB, int max_q_len, float scale, pa_dtype kv_dtype, int* dev_err, void* stream) {
+    const NvtxRange nvtx_range("pa_prefill");
     g_msg[0] = 0;
     if (!kv_dtype_ok(kv_dtype)) return fail(PA_ERR_UNSUPPORTED, "kv_dtype must be F16 or BF16");
     if (out_dtype != PA_F32 && out_dtype != kv_dtype)
@@ -292,6 +322,7 @@ pa_status pa_prefill(void* out, pa_dtype out_dtype, const void* q, const void* p
 pa_status pa_partition_reduce(void* out, pa_dtype out_dtype, const float* part_m2, const float* part_l,
                               const float* part_acc, const int32_t* nparts, int R, int P, int D, int* dev_err,
                               void* stream) {
+    const NvtxRange nvtx_range("pa_partition_reduce");
     g_msg[0] = 0;
     if (out_dtype != PA_F32 && out_dtype != PA_F16 && out_dtype != PA_BF16)
         return fail(PA_ERR_UNSUPPORTED, "bad out_dtype");

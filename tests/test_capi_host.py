@@ -241,3 +241,18 @@ def test_swap_rejects_pageable_host_memory_before_any_launch():
     pairs = np.zeros((1, 2), dtype=np.int64)
     st = L.pa_swap_blocks(host.ctypes.data, 4, host.ctypes.data, 4, pairs.ctypes.data, 1, 16, 1, 64, 1, None, None)
     assert st in (pa.PA_ERR_INVALID, pa.PA_ERR_CUDA)
+
+
+def test_nvtx_ranges_can_be_switched_on():
+    """PA_NVTX=1 wraps every device call in an NVTX range (a no-op without a profiler attached)."""
+    import os
+    import subprocess
+    import sys
+    code = ("import paged_kv_cache_302_gb300 as pa; L = pa.load(); "
+            "st = L.pa_decode(None, 2, None, None, None, None, 1, 16, 1, 128, 16, 1, 1, 16, 0.1, 0, None, 0, 1, "
+            "None, None, None); assert st == pa.PA_ERR_UNSUPPORTED, st; "
+            "assert L.pa_reshape_and_cache(None, None, None, None, 0, 4, 4, 1, 8, 1, None, None) == pa.PA_OK")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=dict(os.environ, PA_NVTX="1"),
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
