@@ -329,6 +329,16 @@ pa_status pa_alloc_seq_len(void* alloc, int seq_id, int64_t* out);
 pa_status pa_alloc_refcount(void* alloc, int block, int* out);
 int pa_alloc_num_free(void* alloc);                                   /* -1 for a NULL handle */
 pa_status pa_alloc_free_list(void* alloc, int32_t* out, int cap, int* n); /* next block to hand out first */
+/* Checkpoint / resume of the whole allocator state as a flat int64 array:
+ * {tag, NB, B, nfree, nseq, free stack (bottom first)[nfree], refcounts[NB],
+ * then per sequence in increasing id: id, tokens, nblocks, blocks[nblocks]}.
+ * pa_alloc_export writes *n words (out NULL: only *n; cap < *n:
+ * PA_ERR_INVALID).  pa_alloc_import builds a new handle from such an array
+ * after checking it: every block is either free (listed once, count 0) or
+ * counted exactly as often as the tables name it, and every table has
+ * ceil(tokens / B) blocks; anything else is PA_ERR_INVALID. */
+pa_status pa_alloc_export(void* alloc, int64_t* out, size_t cap, size_t* n);
+pa_status pa_alloc_import(const int64_t* in, size_t n, void** out);
 
 #ifdef __cplusplus
 }

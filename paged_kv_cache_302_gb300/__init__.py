@@ -101,6 +101,8 @@ def _declare(L):
         "pa_alloc_refcount": ([P, i32, P], i32),
         "pa_alloc_num_free": ([P], i32),
         "pa_alloc_free_list": ([P, P, i32, P], i32),
+        "pa_alloc_export": ([P, P, sz, ctypes.POINTER(ctypes.c_size_t)], i32),
+        "pa_alloc_import": ([P, sz, ctypes.POINTER(ctypes.c_void_p)], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -562,6 +564,27 @@ class BlockAllocator:
         got = ctypes.c_int(0)
         _check(self._L.pa_alloc_free_list(self._h, _i32p(out), n, ctypes.byref(got)))
         return out[: got.value]
+
+    def export_state(self):
+        """The whole allocator state as a flat int64 array (pa_alloc_export)."""
+        import numpy as np
+        n = ctypes.c_size_t(0)
+        _check(self._L.pa_alloc_export(self._h, None, 0, ctypes.byref(n)))
+        out = np.zeros(max(n.value, 1), dtype=np.int64)
+        _check(self._L.pa_alloc_export(self._h, _i32p(out), n.value, ctypes.byref(n)))
+        return out[: n.value]
+
+    @classmethod
+    def from_state(cls, state):
+        """A new allocator rebuilt from an export_state() array (pa_alloc_import, which checks it)."""
+        import numpy as np
+        a = np.ascontiguousarray(state, dtype=np.int64)
+        L = load()
+        h = ctypes.c_void_p()
+        _check(L.pa_alloc_import(_i32p(a), a.size, ctypes.byref(h)))
+        obj = cls.__new__(cls)
+        obj.NB, obj.B, obj._h, obj._L = int(a[1]), int(a[2]), h, L
+        return obj
 
 
 __all__ = [name for name in dir() if name.startswith("pa_")] + ["BlockAllocator", "PAError", "load", "version",

@@ -11,6 +11,8 @@
 // The free list is a LIFO stack; every call validates first and then applies,
 // so a failing call leaves the state unchanged.
 #include <algorithm>
+#include <climits>
+#include <cstdint>
 #include <cstring>
 #include <new>
 #include <unordered_map>
@@ -283,6 +285,95 @@ pa_status pa_alloc_free_list(void* alloc, int32_t* out, int cap, int* n) {
     if (n) *n = sz;
     if (sz > cap || (!out && sz)) return fail(PA_ERR_INVALID, "capacity %d < %d", cap, sz);
     for (int i = 0; i < sz; ++i) out[i] = A->free_stack[sz - 1 - i];
+    return PA_OK;
+}
+
+// ----------------------------------------------------------------------------- state export / import
+
+static constexpr int64_t kStateMagic = 0x3141415043;  // tags the flat state layout below
+
+pa_status pa_alloc_export(void* alloc, int64_t* out, size_t cap, size_t* n) {
+    Allocator* A = as_alloc(alloc);
+    if (!A) return fail(PA_ERR_INVALID, "null allocator");
+    std::vector<int> ids;
+    ids.reserve(A->seqs.size());
+    size_t need = 5 + A->free_stack.size() + (size_t)A->NB;
+    for (const auto& kv : A->seqs) {
+        ids.push_back(kv.first);
+        need += 3 + kv.second.blocks.size();
+    }
+    if (n) *n = need;
+    if (!out) return PA_OK;
+    if (cap < need) return fail(PA_ERR_INVALID, "capacity %zu < %zu words", cap, need);
+    std::sort(ids.begin(), ids.end());
+    size_t w = 0;
+    out[w++] = kStateMagic;
+    out[w++] = A->NB;
+    out[w++] = A->B;
+    out[w++] = (int64_t)A->free_stack.size();
+    out[w++] = (int64_t)ids.size();
+    for (int32_t b : A->free_stack) out[w++] = b;  // bottom of the stack first
+    for (int32_t r : A->ref) out[w++] = r;
+    for (int id : ids) {
+        const Seq& q = A->seqs.at(id);
+        out[w++] = id;
+        out[w++] = q.ntok;
+        out[w++] = (int64_t)q.blocks.size();
+        for (int32_t b : q.blocks) out[w++] = b;
+    }
+    return PA_OK;
+}
+
+pa_status pa_alloc_import(const int64_t* in, size_t n, void** out) {
+    if (!in || !out) return fail(PA_ERR_INVALID, "null argument");
+    *out = nullptr;
+    if (n < 5 || in[0] != kStateMagic) return fail(PA_ERR_INVALID, "not an allocator state");
+    const int64_t NB = in[1], B = in[2], nfree = in[3], nseq = in[4];
+    if (NB <= 0 || NB > INT32_MAX || B <= 0 || B > INT32_MAX || nfree < 0 || nfree > NB || nseq < 0)
+        return fail(PA_ERR_INVALID, "bad header");
+    size_t r = 5;
+    if ((size_t)(n - r) < (size_t)nfree + (size_t)NB) return fail(PA_ERR_INVALID, "truncated state");
+    Allocator* A = new (std::nothrow) Allocator;
+    if (!A) return fail(PA_ERR_OOM, "allocator handle");
+    A->NB = (int)NB;
+    A->B = (int)B;
+    A->free_stack.assign(in + r, in + r + nfree);
+    r += nfree;
+    A->ref.assign(in + r, in + r + NB);
+    r += NB;
+    // every block is either free (once, count 0) or counted exactly as often as the tables name it
+    std::vector<int64_t> seen(NB, 0);
+    auto bad = [&](const char* why) {
+        delete A;
+        return fail(PA_ERR_INVALID, "inconsistent allocator state: %s", why);
+    };
+    for (int32_t b : A->free_stack) {
+        if (b < 0 || b >= NB || A->ref[b] != 0 || seen[b]) return bad("free list");
+        seen[b] = -1;
+    }
+    for (int64_t i = 0; i < nseq; ++i) {
+        if (n - r < 3) return bad("truncated sequence");
+        const int64_t id = in[r], ntok = in[r + 1], nb = in[r + 2];
+        r += 3;
+        if (id < 0 || id > INT32_MAX || ntok < 0 || nb != (ntok + B - 1) / B || (size_t)nb > n - r)
+            return bad("sequence header");
+        Seq q;
+        q.ntok = ntok;
+        for (int64_t j = 0; j < nb; ++j) {
+            const int64_t b = in[r + j];
+            if (b < 0 || b >= NB || seen[b] < 0) return bad("table entry");
+            ++seen[b];
+            q.blocks.push_back((int32_t)b);
+        }
+        r += nb;
+        if (!A->seqs.emplace((int)id, std::move(q)).second) return bad("duplicate sequence");
+    }
+    if (r != n) return bad("trailing words");
+    for (int64_t b = 0; b < NB; ++b) {
+        if (seen[b] == 0) return bad("a block neither free nor in a table");
+        if (seen[b] > 0 && seen[b] != A->ref[b]) return bad("reference count");
+    }
+    *out = A;
     return PA_OK;
 }
 

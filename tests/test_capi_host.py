@@ -256,3 +256,75 @@ def test_nvtx_ranges_can_be_switched_on():
     r = subprocess.run([sys.executable, "-c", code], cwd=root, env=dict(os.environ, PA_NVTX="1"),
                        capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
+
+
+def _observe(a, ids):
+    return (list(a.free_list()), a.num_free(), [list(a.block_table(s)) for s in ids], [a.seq_len(s) for s in ids],
+            [a.refcount(b) for b in range(a.NB)])
+
+
+def _mixed_state(NB=48, B=4, seed=60):
+    rng = np.random.default_rng(seed)
+    a = pa.BlockAllocator(NB, B, rng.permutation(NB))
+    for s in range(4):
+        a.add_seq(s)
+        a.append_slots(s, int(rng.integers(1, 11)))
+    a.fork(0, 10)
+    a.fork(10, 11)                      # a shared partial block with count 3
+    a.append_slots(11, 3)               # copy-on-write
+    a.free_seq(2)
+    return a, [0, 1, 3, 10, 11]
+
+
+def test_allocator_state_round_trips_and_continues_identically():
+    a, ids = _mixed_state()
+    state = a.export_state()
+    b = pa.BlockAllocator.from_state(state)
+    assert _observe(b, ids) == _observe(a, ids)
+    assert np.array_equal(b.export_state(), state)
+    for x in (a, b):                    # the same operations on the original and the resumed allocator
+        x.append_slots(0, 5)
+        x.add_seq(20)
+        x.append_slots(20, 9)
+        x.fork(20, 21)
+        x.free_seq(1)
+    for s in (0, 20, 21, 10, 11):
+        assert list(a.append_slots(s, 2)[0]) == list(b.append_slots(s, 2)[0])
+    ids = [0, 3, 10, 11, 20, 21]
+    assert _observe(b, ids) == _observe(a, ids)
+
+
+def test_allocator_import_rejects_inconsistent_states():
+    a, _ = _mixed_state()
+    good = a.export_state()
+    NB, nfree = int(good[1]), int(good[3])
+    free0, ref0 = 5, 5 + nfree
+    used = [b for b in range(NB) if good[ref0 + b] > 0]
+
+    def bad(mut):
+        s = good.copy()
+        s = mut(s)
+        with pytest.raises(pa.PAError) as e:
+            pa.BlockAllocator.from_state(s)
+        assert e.value.status == pa.PA_ERR_INVALID
+
+    bad(lambda s: np.concatenate([[0], s[1:]]))                            # not a state
+    bad(lambda s: np.concatenate([s, [0]]))                                # trailing word
+    bad(lambda s: s[:-1])                                                  # truncated
+    def dup_free(s):
+        s[free0 + 1] = s[free0]
+        return s
+    bad(dup_free)                                                          # a block listed free twice
+    def ref_off(s):
+        s[ref0 + used[0]] += 1
+        return s
+    bad(ref_off)                                                           # count disagrees with the tables
+    def drop_free(s):
+        s[3] -= 1
+        return np.delete(s, free0)
+    bad(drop_free)                                                         # a block neither free nor used
+    def wrong_len(s):
+        seq0 = ref0 + NB
+        s[seq0 + 1] += 4 * int(s[2])                                       # tokens no longer match the blocks
+        return s
+    bad(wrong_len)
