@@ -29,6 +29,8 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+# A prebuilt library to load instead (the mutation tests point this at deliberately broken copies).
+_LIB_OVERRIDE = os.environ.get("ORACLE_LIB")
 _lock = threading.Lock()
 _lib = None
 
@@ -37,6 +39,8 @@ F16, BF16 = 0, 1
 
 def build(force: bool = False) -> str:
     """Compile ``oracle.c`` into ``_build/liboracle.so`` (gcc, -O2, OpenMP)."""
+    if _LIB_OVERRIDE:
+        return _LIB_OVERRIDE
     os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
@@ -53,8 +57,7 @@ def lib():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            L = ctypes.CDLL(_LIB_PATH)
+            L = ctypes.CDLL(build())
             P = ctypes.c_void_p
             i32, i64, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_double
             L.oracle_half_to_double.argtypes = [ctypes.c_uint16]
