@@ -222,19 +222,24 @@ def test_contiguous_layout_matches_paged_bit_for_bit_and_oracle():
         C.assert_close(out.cpu().numpy(), ref, f"contiguous pt={pt}")
 
 
-def test_low_precision_output_is_the_rounded_fp32_output():
-    """bf16 output = round-to-nearest-even of the fp32 output of the same call, bit for bit,
-    and within the fp32 tolerance plus half a bf16 ulp of the oracle."""
-    w = W.llama3_8b(n_seqs=10)
+@pytest.mark.parametrize("make", [lambda: W.llama3_8b(n_seqs=10), lambda: W.opt13b(n_seqs=6)],
+                         ids=["bf16", "fp16"])
+def test_low_precision_output_is_the_rounded_fp32_output(make):
+    """A 16-bit output = round-to-nearest-even of the fp32 output of the same call, bit for bit, and within the
+    fp32 tolerance plus half an ulp of the oracle: unpartitioned, 512-token partitions (warp-per-row merge) and
+    32-token partitions (at least 32 per row: CTA-per-row merge)."""
+    w = make()
     c = C.build_paged(w)
     ref = C.oracle_decode(c)
-    for pt in (0, -1):
+    odt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+    assert (int(c.ctx.max()) + 31) // 32 >= 32
+    for pt in (0, -1, 32):
         out32 = C.gpu_decode(c, partition_tokens=pt).cpu().numpy()
-        out16 = C.gpu_decode(c, partition_tokens=pt, out_dtype=torch.bfloat16)
+        out16 = C.gpu_decode(c, partition_tokens=pt, out_dtype=odt)
         bits = C.to_bits(out16)
-        assert np.array_equal(bits, W.round_bits(out32, "bf16"))
-        half_ulp = np.abs(W.bits_to_float(bits + 1, "bf16") - W.bits_to_float(bits, "bf16")) / 2
-        assert np.all(np.abs(W.bits_to_float(bits, "bf16") - ref) <= C.ATOL + half_ulp)
+        assert np.array_equal(bits, W.round_bits(out32, w.dtype))
+        half_ulp = np.abs(W.bits_to_float(bits + 1, w.dtype) - W.bits_to_float(bits, w.dtype)) / 2
+        assert np.all(np.abs(W.bits_to_float(bits, w.dtype) - ref) <= C.ATOL + half_ulp)
 
 
 @pytest.mark.parametrize("R,P,D", [(37, 9, 128), (37, 40, 128), (11, 300, 128), (23, 33, 64)])
