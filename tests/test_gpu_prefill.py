@@ -81,3 +81,20 @@ def test_prefill_large_chunks_sampled_rows():
     o = out.cpu().numpy().reshape(-1, w.D)[rows]
     C.assert_close(o, ref.reshape(-1, w.D)[rows], "prefill large")
     assert np.all(np.isfinite(out.cpu().numpy()))
+
+
+@pytest.mark.parametrize("make,ctx,chunks", [
+    (lambda: W.llama3_8b(n_seqs=3), [300, 129, 700], [300, 50, 129]),    # bf16
+    (lambda: W.opt13b(n_seqs=2), [200, 513], [200, 77]),                  # fp16
+], ids=["bf16", "fp16"])
+def test_prefill_low_precision_output_is_the_rounded_fp32_output(make, ctx, chunks):
+    """A 16-bit prefill output is the round-to-nearest-even of the fp32 output of the same inputs, bit for bit."""
+    c = C.build_paged(_with_ctx(make(), ctx))
+    w = c.w
+    out32, ref, _, _ = _run(c, chunks)
+    odt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+    out16, _, _, _ = _run(c, chunks, out_dtype=odt)
+    bits = C.to_bits(out16)
+    assert np.array_equal(bits, W.round_bits(out32.cpu().numpy(), w.dtype))
+    half_ulp = np.abs(W.bits_to_float(bits + 1, w.dtype) - W.bits_to_float(bits, w.dtype)) / 2
+    assert np.all(np.abs(W.bits_to_float(bits, w.dtype) - ref) <= C.ATOL + half_ulp)
