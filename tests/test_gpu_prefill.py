@@ -98,3 +98,30 @@ def test_prefill_low_precision_output_is_the_rounded_fp32_output(make, ctx, chun
     assert np.array_equal(bits, W.round_bits(out32.cpu().numpy(), w.dtype))
     half_ulp = np.abs(W.bits_to_float(bits + 1, w.dtype) - W.bits_to_float(bits, w.dtype)) / 2
     assert np.all(np.abs(W.bits_to_float(bits, w.dtype) - ref) <= C.ATOL + half_ulp)
+
+
+def test_prefill_device_errors_are_flagged_not_faulted():
+    """A block id outside the pool is flagged (its copy reads zeros) and a chunk longer than its context is flagged
+    and not computed; the context stays usable and the next call is exact."""
+    w = _with_ctx(W.llama3_8b(n_seqs=3), [300, 129, 700])
+    c = C.build_paged(w)
+    chunks = [300, 50, 129]
+    q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    T = int(q_start[-1])
+    q = W.normal_bits(np.random.default_rng(0), (T, w.H_q, w.D), w.dtype)
+    tab, ctx = c.dev_tables()
+    out = torch.zeros((T, w.H_q, w.D), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bad_tab = tab.clone()
+    bad_tab[1, 0] = w.NB + 7
+    pa.pa_prefill(out, C.to_dev(q, w.dtype), c.pool, bad_tab, ctx, torch.from_numpy(q_start).cuda(), 300, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() & pa.PA_DEV_ERR_BLOCK
+    err.zero_()
+    bad_ctx = ctx.clone()
+    bad_ctx[2] = 100                                     # a 129-token chunk cannot end a 100-token context
+    pa.pa_prefill(out, C.to_dev(q, w.dtype), c.pool, tab, bad_ctx, torch.from_numpy(q_start).cuda(), 300, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() & pa.PA_DEV_ERR_CTX
+    out2, ref, _, _ = _run(c, chunks)
+    C.assert_close(out2.cpu().numpy(), ref, "prefill after flagged calls")
