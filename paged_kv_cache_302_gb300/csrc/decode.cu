@@ -8,7 +8,7 @@
 // リクエスト単位のKVキャッシュインデキシング (request r at offset r * S).
 //
 // Three kernels per call:
-//  1. plan_kernel (1 CTA; plan_coop_kernel up to 128 sequences): splits every
+//  1. plan_kernel (one CTA per slice of consecutive sequences): splits every
 //     context into partitions of PT tokens and writes one work record (seq, kv
 //     head, partition, ctx) per (partition, kv head) in longest-first order:
 //     whole partitions in sequence order, then the ragged last partitions by
@@ -41,7 +41,6 @@ namespace pa {
 
 constexpr int kNumBins = 2048;
 constexpr int kPlanThreads = 1024;
-constexpr int kPlanChunk = 4096;  // sequences whose partition offsets sit in shared memory at once
 constexpr int kAttnThreads = 64;
 constexpr uint32_t kSwzRowBytes = 128;
 
@@ -126,19 +125,32 @@ static int plan_bins(int PT, int max_ctx) {
     return n < kNumBins ? n : kNumBins;
 }
 
+// The schedule is written by several CTAs.  CTA j owns the sequences [j*S, min(N, (j+1)*S)) and writes only their
+// records, so the record stores of a call spread over the grid instead of queueing in one SM (a one-CTA schedule
+// took about 16K cycles for the 7.9K records of 256 Llama-3-8B-shaped sequences).  To place its slice a CTA reads every
+// context length: its first whole partition follows the whole partitions of all earlier sequences, and its
+// ragged tails of one length bin follow that bin's tails from earlier slices.  Inside a CTA each warp writes whole
+// sequences' records with its lanes on consecutive records, so a long sequence's P * H_kv records do not queue up
+// behind one thread.  Within a (slice, bin) the tails' order is that of the atomic increments.
+constexpr int kPlanSlice = 32;  // sequences per CTA while the grid still fits on the SMs
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ ctx_lens,
-                                                            const int32_t* __restrict__ req_ids, int N, int H_kv,
-                                                            int PT, int max_ctx, int cap, int N_max, int nbins,
-                                                            int* __restrict__ header, int4* __restrict__ rec,
-                                                            int* __restrict__ nparts, int* err) {
+                                                                  const int32_t* __restrict__ req_ids, int N,
+                                                                  int H_kv, int PT, int max_ctx, int cap, int N_max,
+                                                                  int nbins, int* __restrict__ header,
+                                                                  int4* __restrict__ rec, int* __restrict__ nparts,
+                                                                  int* err) {
     griddep_wait();
     griddep_launch_dependents();
-    __shared__ int bins[kNumBins];
-    __shared__ int warp_sum[32];
+    __shared__ int bins[kNumBins];       // tails per bin over all sequences, then this slice's next tail slot per bin
+    __shared__ int before[kNumBins];     // tails per bin over the sequences before the slice
+    __shared__ int pre[kPlanThreads];    // per sequence of a chunk: global index of its first whole partition
+    __shared__ int cctx[kPlanThreads];   // per sequence of a chunk: checked context length (0: invalid)
+    __shared__ int warp_sum[2][32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    for (int b = tid; b < nbins; b += blockDim.x) bins[b] = 0;
-    const int per = (N + blockDim.x - 1) / blockDim.x;
-    const int s_begin = min(N, tid * per), s_end = min(N, s_begin + per);
+    const int S = (N + gridDim.x - 1) / gridDim.x;
+    const int lo = min(N, (int)blockIdx.x * S), n = min(N, lo + S) - lo;
+    for (int b = tid; b < nbins; b += blockDim.x) bins[b] = before[b] = 0;
     // context length of sequence s, 0 for an invalid length, -1 for an invalid request id
     auto checked_ctx = [&](int s) -> int {
         const int c = ctx_lens[s];
@@ -151,179 +163,87 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     };
     __syncthreads();
 
-    // pass 1: whole partitions per thread, histogram of ragged tails
-    int my_full = 0;
-    for (int s = s_begin; s < s_end; ++s) {
-        const int c = checked_ctx(s);
-        if (c <= 0) {
+    // pass 1 over every sequence: whole partitions in total and before the slice, tail histograms; the slice's
+    // partition counts and error flags
+    // (whole warps step together so that lanes of one bin add their count with one atomic)
+    int full_all = 0, full_before = 0;
+    for (int s0 = warp * 32; s0 < N; s0 += blockDim.x) {
+        const int s = s0 + lane;
+        const int c = s < N ? checked_ctx(s) : 0;
+        const bool mine = s >= lo && s < lo + n;
+        if (c <= 0 && mine) {
             flag_error(err, c == 0 ? PA_DEV_ERR_CTX : PA_DEV_ERR_REQ);
             nparts[s] = 0;
-            continue;
         }
-        const int nf = c / PT, rem = c - nf * PT;
-        nparts[s] = nf + (rem > 0);
-        my_full += nf;
-        if (rem > 0) atomicAdd(&bins[size_bin(rem, nbins)], 1);
+        const int nf = c > 0 ? c / PT : 0, rem = c > 0 ? c - nf * PT : 0;
+        full_all += nf;
+        if (s < lo) full_before += nf;
+        if (mine && c > 0) nparts[s] = nf + (rem > 0);
+        const int b = rem > 0 ? size_bin(rem, nbins) : -1;
+        const unsigned same = __match_any_sync(0xffffffffu, b);
+        if (b >= 0 && lane == __ffs(same) - 1) atomicAdd(&bins[b], __popc(same));
+        const int bb = s < lo ? b : -1;
+        const unsigned same_before = __match_any_sync(0xffffffffu, bb);
+        if (bb >= 0 && lane == __ffs(same_before) - 1) atomicAdd(&before[bb], __popc(same_before));
     }
-
-    // exclusive scan of whole partitions in sequence order
-    const int incl = warp_incl_scan(my_full);
-    if (lane == 31) warp_sum[warp] = incl;
+    full_all = __reduce_add_sync(0xffffffffu, full_all);
+    full_before = __reduce_add_sync(0xffffffffu, full_before);
+    if (lane == 0) {
+        warp_sum[0][warp] = full_all;
+        warp_sum[1][warp] = full_before;
+    }
     __syncthreads();
     if (warp == 0) {
-        int v = lane < nwarps ? warp_sum[lane] : 0;
-        v = warp_incl_scan(v);
-        warp_sum[lane] = v;
-    }
-    __syncthreads();
-    const int full_total = warp_sum[nwarps - 1];
-    int full_pos = incl - my_full + (warp ? warp_sum[warp - 1] : 0);
-    __syncthreads();
-
-    // descending exclusive scan of the tail histogram: longest tails first
-    if (warp == 0) {
+        const int t = __reduce_add_sync(0xffffffffu, lane < nwarps ? warp_sum[0][lane] : 0);
+        const int f = __reduce_add_sync(0xffffffffu, lane < nwarps ? warp_sum[1][lane] : 0);
+        // descending exclusive scan of the tail histogram: longest tails first, after all whole partitions; the
+        // slice's tails of a bin start after the earlier slices' tails of that bin
         const int chunk = (nbins + 31) / 32;
         int sum = 0;
         for (int j = lane * chunk; j < min(nbins, (lane + 1) * chunk); ++j) sum += bins[nbins - 1 - j];
         const int tincl = warp_incl_scan(sum);
-        int run = full_total + tincl - sum;
+        int run = t + tincl - sum;
         for (int j = lane * chunk; j < min(nbins, (lane + 1) * chunk); ++j) {
-            const int c = bins[nbins - 1 - j];
-            bins[nbins - 1 - j] = run;
+            const int b = nbins - 1 - j, c = bins[b];
+            bins[b] = run + before[b];
             run += c;
         }
-        if (lane == 31) header[0] = (full_total + tincl) * H_kv;
+        if (lane == 31 && blockIdx.x == 0) header[0] = (t + tincl) * H_kv;
+        if (lane == 0) warp_sum[1][0] = f;
     }
     __syncthreads();
+    int base = warp_sum[1][0];  // whole partitions before the current chunk of the slice
 
-    // pass 2: one record per (partition, kv head)
-    for (int s = s_begin; s < s_end; ++s) {
-        const int c = checked_ctx(s);
-        if (c <= 0) continue;
-        const int nf = c / PT, rem = c - nf * PT;
-        for (int p = 0; p < nf; ++p, ++full_pos)
-            for (int h = 0; h < H_kv; ++h) rec[(size_t)full_pos * H_kv + h] = make_int4(s, h, p, c);
-        if (rem > 0) {
-            const int pos = atomicAdd(&bins[size_bin(rem, nbins)], 1);
-            for (int h = 0; h < H_kv; ++h) rec[(size_t)pos * H_kv + h] = make_int4(s, h, nf, c);
-        }
-    }
-}
-
-// The same schedule for few sequences (N <= kCoopPlanSeqs): each warp writes whole sequences' records with its lanes
-// on consecutive records, so a long sequence's P * H_kv records do not queue up behind one thread (measured on one
-// box: 8 x 32K Yi-34B whole call +3.5 %, 64-sequence OPT-13B +1.5 %; at 256 sequences the extra scan cost ~1 %).
-constexpr int kCoopPlanSeqs = 128;
-
-__global__ void __launch_bounds__(kPlanThreads) plan_coop_kernel(const int32_t* __restrict__ ctx_lens,
-                                                            const int32_t* __restrict__ req_ids, int N, int H_kv,
-                                                            int PT, int max_ctx, int cap, int N_max, int nbins,
-                                                            int* __restrict__ header, int4* __restrict__ rec,
-                                                            int* __restrict__ nparts, int* err) {
-    griddep_wait();
-    griddep_launch_dependents();
-    __shared__ int bins[kNumBins];
-    __shared__ int pre[kPlanChunk];    // per chunk: global index of each sequence's first whole partition
-    __shared__ int cctx[kPlanChunk];   // per chunk: checked context lengths (0: invalid)
-    __shared__ int warp_sum[32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    for (int b = tid; b < nbins; b += blockDim.x) bins[b] = 0;
-    // context length of sequence s, 0 for an invalid length, -1 for an invalid request id
-    auto checked_ctx = [&](int s) -> int {
-        const int c = ctx_lens[s];
-        if (c < 1 || c > max_ctx || c > cap) return 0;
-        if (req_ids) {
-            const int r = req_ids[s];
-            if (r < 0 || r >= N_max) return -1;
-        }
-        return c;
-    };
-    // exclusive block scan of one value per thread (in thread order); also returns the total
-    auto block_excl_scan = [&](int v, int& total) {
+    // pass 2 over the slice, blockDim.x sequences at a time: an exclusive scan gives each sequence the index of its
+    // first whole partition, then each warp writes whole sequences' records (one per (partition, kv head))
+    for (int c0 = 0; c0 < n; c0 += blockDim.x) {
+        const int m = min((int)blockDim.x, n - c0);
+        int c = tid < m ? checked_ctx(lo + c0 + tid) : 0;
+        c = c > 0 ? c : 0;
+        if (tid < m) cctx[tid] = c;
+        const int v = c / PT;
         const int incl = warp_incl_scan(v);
         __syncthreads();
-        if (lane == 31) warp_sum[warp] = incl;
+        if (lane == 31) warp_sum[0][warp] = incl;
         __syncthreads();
-        if (warp == 0) {
-            int x = lane < nwarps ? warp_sum[lane] : 0;
-            warp_sum[lane] = warp_incl_scan(x);
-        }
+        if (warp == 0) warp_sum[0][lane] = warp_incl_scan(lane < nwarps ? warp_sum[0][lane] : 0);
         __syncthreads();
-        total = warp_sum[nwarps - 1];
-        return incl - v + (warp ? warp_sum[warp - 1] : 0);
-    };
-    __syncthreads();
-
-    // pass 1: partition counts, whole partitions in total, histogram of ragged tails
-    int my_full = 0;
-    for (int s = tid; s < N; s += blockDim.x) {
-        const int c = checked_ctx(s);
-        if (c <= 0) {
-            flag_error(err, c == 0 ? PA_DEV_ERR_CTX : PA_DEV_ERR_REQ);
-            nparts[s] = 0;
-            continue;
-        }
-        const int nf = c / PT, rem = c - nf * PT;
-        nparts[s] = nf + (rem > 0);
-        my_full += nf;
-        if (rem > 0) atomicAdd(&bins[size_bin(rem, nbins)], 1);
-    }
-    int full_total;
-    block_excl_scan(my_full, full_total);
-
-    // descending exclusive scan of the tail histogram: longest tails first, after all whole partitions
-    if (warp == 0) {
-        const int chunk = (nbins + 31) / 32;
-        int sum = 0;
-        for (int j = lane * chunk; j < min(nbins, (lane + 1) * chunk); ++j) sum += bins[nbins - 1 - j];
-        const int tincl = warp_incl_scan(sum);
-        int run = full_total + tincl - sum;
-        for (int j = lane * chunk; j < min(nbins, (lane + 1) * chunk); ++j) {
-            const int c = bins[nbins - 1 - j];
-            bins[nbins - 1 - j] = run;
-            run += c;
-        }
-        if (lane == 31) header[0] = (full_total + tincl) * H_kv;
-    }
-    __syncthreads();
-
-    // pass 2, a chunk of sequences at a time.  Each thread scans a run of consecutive sequences, giving every
-    // sequence the index of its first whole partition; then each warp writes whole sequences' records, its
-    // lanes on consecutive records (one record per (partition, kv head), partitions in sequence order, the
-    // ragged tail at its slot of the length-sorted tail list), so a long sequence's records do not queue up
-    // behind one thread.
-    int base = 0;  // whole partitions of the chunks before this one
-    for (int c0 = 0; c0 < N; c0 += kPlanChunk) {
-        const int n = min(kPlanChunk, N - c0);
-        const int per = (n + blockDim.x - 1) / blockDim.x;
-        const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
-        int run = 0;
-        for (int i = i0; i < i1; ++i) {
-            const int c = checked_ctx(c0 + i);
-            cctx[i] = c > 0 ? c : 0;
-            run += (c > 0 ? c : 0) / PT;
-        }
-        int chunk_total;
-        int first = base + block_excl_scan(run, chunk_total);
-        for (int i = i0; i < i1; ++i) {
-            pre[i] = first;
-            first += cctx[i] / PT;
-        }
+        if (tid < m) pre[tid] = base + incl - v + (warp ? warp_sum[0][warp - 1] : 0);
+        base += warp_sum[0][nwarps - 1];
         __syncthreads();
-        for (int i = warp; i < n; i += nwarps) {
-            const int c = cctx[i];
-            if (c == 0) continue;
-            const int s = c0 + i, nf = c / PT, rem = c - nf * PT;
+        for (int i = warp; i < m; i += nwarps) {
+            const int ci = cctx[i];
+            if (ci == 0) continue;
+            const int s = lo + c0 + i, nf = ci / PT, rem = ci - nf * PT;
             int4* r0 = rec + (size_t)pre[i] * H_kv;
-            for (int k = lane; k < nf * H_kv; k += 32) r0[k] = make_int4(s, k % H_kv, k / H_kv, c);
+            for (int k = lane; k < nf * H_kv; k += 32) r0[k] = make_int4(s, k % H_kv, k / H_kv, ci);
             if (rem > 0) {
                 int pos = 0;
                 if (lane == 0) pos = atomicAdd(&bins[size_bin(rem, nbins)], 1);
                 pos = __shfl_sync(0xffffffffu, pos, 0);
-                for (int h = lane; h < H_kv; h += 32) rec[(size_t)pos * H_kv + h] = make_int4(s, h, nf, c);
+                for (int h = lane; h < H_kv; h += 32) rec[(size_t)pos * H_kv + h] = make_int4(s, h, nf, ci);
             }
         }
-        base += chunk_total;
         __syncthreads();
     }
 }
@@ -1075,8 +995,12 @@ pa_status launch_decode(const DecodeArgs& a) {
     int* nparts = reinterpret_cast<int*>(ws + L.nparts);
     int4* rec = reinterpret_cast<int4*>(ws + L.records);
     const int cap = a.paged ? a.MB * a.B : a.S_max;
-    cudaError_t e = launch_kernel(a.N <= kCoopPlanSeqs ? plan_coop_kernel : plan_kernel, dim3(1), dim3(kPlanThreads), 0,
-                                  a.stream, a.ctx_lens,
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // kPlanSlice sequences per CTA, at most one CTA per SM (larger slices beyond that)
+    const int plan_ctas = std::min((a.N + kPlanSlice - 1) / kPlanSlice, std::max(sms, 1));
+    cudaError_t e = launch_kernel(plan_kernel, dim3(plan_ctas), dim3(kPlanThreads), 0, a.stream, a.ctx_lens,
                                   a.paged ? nullptr : a.req_ids, a.N, a.H_kv, L.PT, a.max_ctx, cap, a.N_max,
                                   plan_bins(L.PT, a.max_ctx), header, rec, nparts, a.dev_err);
     count_launch();

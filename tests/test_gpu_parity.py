@@ -179,6 +179,73 @@ def test_many_short_sequences_every_output():
         C.assert_close(C.gpu_decode(c, partition_tokens=pt).cpu().numpy(), ref, f"many short pt={pt}")
 
 
+def _schedule_view(ws, N, maxrec):
+    """(records [n, 4] int32 rows (seq, kv head, partition, ctx), per-sequence partition counts) that a decode call
+    left in its workspace.  White box: the workspace holds a 16-byte header (record count in word 0), the
+    per-sequence partition counts and the records, each part starting on a 256-byte boundary."""
+    off = (256 + 4 * N + 255) // 256 * 256
+    b = ws[: off + 16 * maxrec].cpu().numpy()
+    total = int(b[:4].view(np.int32)[0])
+    assert 0 <= total <= maxrec
+    return b[off: off + 16 * total].view(np.int32).reshape(total, 4), b[256: 256 + 4 * N].view(np.int32).copy()
+
+
+@pytest.mark.parametrize("N,H_kv,pt,max_len", [(1, 8, 0, 3000), (33, 8, 0, 3000), (256, 8, 0, 8192),
+                                                 (5000, 2, 64, 200), (40000, 1, -1, 700), (200000, 1, 32, 60)],
+                         ids=["1", "33", "256", "5000-pt64", "40000-whole", "200000-pt32"])
+def test_schedule_covers_every_work_item_once_longest_first(N, H_kv, pt, max_len):
+    """The schedule's work records, read back from a poisoned workspace: exactly one per (sequence, kv head,
+    partition); the whole partitions first, in (sequence, partition, kv head) order; then each ragged last
+    partition as H_kv consecutive records, by non-increasing length in bins of one 32-token stage.  The batches
+    run from one CTA to one per SM, with slices above 1024 sequences at the largest size.  Sampled outputs match
+    the oracle (the tables point into a small shared pool, so sequences share blocks)."""
+    rng = np.random.default_rng(N)
+    B, D, H_q, NB = 16, 64, 2 * H_kv, 64
+    PT = {0: 512, -1: 1 << 30}.get(pt, pt)
+    ctx = rng.integers(1, max_len + 1, size=N).astype(np.int32)
+    ctx[0] = max_len
+    MB = (max_len + B - 1) // B
+    tables = rng.integers(0, NB, size=(N, MB)).astype(np.int32)
+    pool_bits = W.normal_bits(rng, (NB, B, 2, H_kv, D), "f16")
+    q_bits = W.normal_bits(rng, (N, H_q, D), "f16")
+    ws = torch.full((pa.pa_decode_workspace_bytes(N, H_q, H_kv, D, max_len, pt),), 0xAB, dtype=torch.uint8,
+                    device="cuda")
+    out = torch.empty((N, H_q, D), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_decode(out, C.to_dev(q_bits, "f16"), C.to_dev(pool_bits, "f16"), torch.from_numpy(tables).cuda(),
+                 torch.from_numpy(ctx).cuda(), max_len, partition_tokens=pt, workspace=ws, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    P = (ctx.astype(np.int64) + PT - 1) // PT
+    rec, nparts = _schedule_view(ws, N, int(P.sum()) * H_kv)
+    assert np.array_equal(nparts, P)
+    s, h, p, c = (x.astype(np.int64) for x in rec.T)
+    assert rec.shape[0] == P.sum() * H_kv
+    assert np.array_equal(c, ctx[s])
+    keys = np.sort((s * H_kv + h) * P.max() + p)
+    seq = np.repeat(np.arange(N), P * H_kv)
+    part = np.concatenate([np.repeat(np.arange(n), H_kv) for n in P])
+    want = np.sort((seq * H_kv + np.tile(np.arange(H_kv), int(P.sum()))) * P.max() + part)
+    assert np.array_equal(keys, want), "some work item is missing or repeated"
+    nf = ctx.astype(np.int64) // PT
+    F = int(nf.sum()) * H_kv
+    whole = (p + 1) * PT <= c
+    assert whole[:F].all() and not whole[F:].any()
+    ws_seq = np.repeat(np.arange(N), nf * H_kv)
+    ws_part = np.concatenate([np.repeat(np.arange(n), H_kv) for n in nf]) if F else np.zeros(0, np.int64)
+    assert np.array_equal(s[:F], ws_seq) and np.array_equal(p[:F], ws_part)
+    assert np.array_equal(h[:F], np.tile(np.arange(H_kv), F // H_kv))
+    ts, th = s[F:].reshape(-1, H_kv), h[F:].reshape(-1, H_kv)
+    assert (ts == ts[:, :1]).all() and (th == np.arange(H_kv)).all()
+    bins = (c[F:] - p[F:] * PT + 31) // 32
+    assert np.all(np.diff(bins) <= 0), "ragged partitions out of longest-first order"
+    pick = np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, size=22)]))
+    pairs = np.array([(x, y) for x in pick for y in (0, H_q - 1)], dtype=np.int32)
+    ref = oracle.paged_decode(q_bits, pool_bits, tables, ctx, "f16", pairs=pairs)
+    got = out.cpu().numpy()
+    C.assert_close(got[pairs[:, 0], pairs[:, 1]], ref[pairs[:, 0], pairs[:, 1]], f"schedule N={N}")
+
+
 def test_block_relabelling_gives_identical_bits():
     w = W.llama3_8b(n_seqs=12)
     c = C.build_paged(w, check_pool=False)
