@@ -276,7 +276,7 @@ def attend_source_sha256() -> str:
     """Hash of the attention kernel's source: its template in decode.cu plus the device helpers."""
     src = open(DECODE_SRC).read()
     a = src.index("// ============================================================================= 2. attention")
-    b = src.index("// ============================================================================= merge of partition")
+    b = src.index("// ============================================================================= 3. partition merge")
     return hashlib.sha256((src[a:b] + open(DEVICE_HDR).read()).encode()).hexdigest()
 
 

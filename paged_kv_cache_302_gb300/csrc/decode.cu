@@ -13,8 +13,9 @@
 //     head, partition, ctx) per (partition, kv head) in longest-first order:
 //     whole partitions in sequence order, then the ragged last partitions by
 //     decreasing length.
-//  2. attend_kernel (persistent, 4 CTAs per SM, 2 warps each): CTA c takes
-//     records c, c + grid, ...  Warp 1 (producer) streams each record's K/V
+//  2. attend_kernel (persistent, 4 CTAs per SM, 2 warps each): CTA c takes the
+//     whole-partition records c, c + grid, ..., then ragged tails from a shared
+//     counter, longest first.  Warp 1 (producer) streams each record's K/V
 //     through a ring of shared-memory stages with TMA: one 5-D tensor copy per
 //     KV block brings the block's K and V rows of one head, 128-byte swizzled;
 //     the first stage of a record also carries the record's G query rows.
@@ -77,7 +78,7 @@ bool workspace_layout(int N, int H_q, int H_kv, int D, int max_ctx, int partitio
         return false;
     const int P = PT >= kUnpartitioned ? 1 : (max_ctx + PT - 1) / PT;
     size_t off = 0;
-    L->header = off;
+    L->header = off;  // record count, tail counter, whole-partition record count
     off = align256(off + 16);
     L->nparts = off;
     off = align256(off + sizeof(int) * (size_t)N);
@@ -208,7 +209,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
             bins[b] = run + before[b];
             run += c;
         }
-        if (lane == 31 && blockIdx.x == 0) header[0] = (t + tincl) * H_kv;
+        if (lane == 31 && blockIdx.x == 0) {
+            header[0] = (t + tincl) * H_kv;
+            header[1] = 0;
+            header[2] = t * H_kv;
+        }
         if (lane == 0) warp_sum[1][0] = f;
     }
     __syncthreads();
@@ -266,7 +271,7 @@ __device__ __forceinline__ void store_row(OutT* dst, const float (&o)[D / 32]) {
 
 struct AttnParams {
     const int4* rec;
-    const int* header;
+    int* header;
     const int32_t* tables;
     int MB, B, NB;
     const int32_t* req_ids;
@@ -339,16 +344,29 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
 
     if (threadIdx.x >= 32) {
         // ------------------------------------------------------------------ producer warp
-        const int total = p.header[0];
+        const int total = p.header[0], nwhole = p.header[2];
         const uint64_t pol = policy_evict_first();
         const int bps = kStageTok / Beff;  // boxes per stage
         int slot = 0;
         uint32_t ephase = 0;
         bool ok = true;
-        int idx = blockIdx.x;
         const int4 none = make_int4(-1, 0, 0, 0);
-        int4 cur = idx < total ? p.rec[idx] : none;
-        int4 nxt = idx + (int)gridDim.x < total ? p.rec[idx + gridDim.x] : none;
+        // record order: the whole partitions round robin (CTA c takes c, c + grid, ... below nwhole), then the
+        // ragged tails from a shared counter, so the CTAs that run out of whole partitions first take the
+        // longest tails; lane 0 asks for the index after the next record while the current one streams
+        auto after = [&](int i) -> int {
+            const int j = i + (int)gridDim.x;
+            return j < nwhole ? j : nwhole + atomicAdd(p.header + 1, 1);
+        };
+        int nidx = 0;
+        if (lane == 0) nidx = after((int)blockIdx.x - (int)gridDim.x);
+        nidx = __shfl_sync(0xffffffffu, nidx, 0);
+        int4 cur = nidx < total ? p.rec[nidx] : none;
+        if (lane == 0) nidx = after(nidx);
+        nidx = __shfl_sync(0xffffffffu, nidx, 0);
+        int4 nxt = nidx < total ? p.rec[nidx] : none;
+        int pend = 0;
+        if (lane == 0 && nxt.x >= 0) pend = after(nidx);
         // table entries of the first 32 boxes of `it` starting at box `cb`
         auto load_entries = [&](const int4& it, int cb) -> int {
             const int t0 = it.z * p.PT;
@@ -425,9 +443,10 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
                 }
                 ent = ent_nx;
             }
-            idx += gridDim.x;
             cur = nxt;
-            nxt = idx + (int)gridDim.x < total ? p.rec[idx + gridDim.x] : none;
+            nidx = __shfl_sync(0xffffffffu, pend, 0);
+            nxt = nidx < total ? p.rec[nidx] : none;
+            if (lane == 0 && nxt.x >= 0) pend = after(nidx);
         }
         if (ok && lane == 0) {
             ok = mbar_wait_bounded(empty_s + 8 * slot, ephase ^ 1, abort_flag);
@@ -920,7 +939,7 @@ static pa_status run_attend(const DecodeArgs& a, const WorkspaceLayout& L, const
     AttnParams p;
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     p.rec = reinterpret_cast<const int4*>(ws + L.records);
-    p.header = reinterpret_cast<const int*>(ws + L.header);
+    p.header = reinterpret_cast<int*>(ws + L.header);
     p.tables = a.tables;
     p.MB = a.MB;
     p.B = a.B;
