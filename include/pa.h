@@ -144,7 +144,11 @@ size_t pa_decode_workspace_bytes(int N, int H_q, int H_kv, int D, int max_ctx, i
  *     out[s][h] = sum_t softmax(x)_t * V_t,
  * K_t, V_t = pool[block_tables[s][t / B]][t % B][0 / 1][g].
  *
- * out: [N][H_q][D] of out_dtype (F32, F16 or BF16); q: [N][H_q][D] of kv_dtype;
+ * out: [N][H_q][D] of out_dtype (F32, F16 or BF16), in device memory or in
+ * pinned host memory (cudaHostAlloc / cudaHostRegister, addressed through the
+ * same pointer): the kernels then write each output row across the host link
+ * as it completes, which replaces a separate device-to-host copy of the
+ * result; q: [N][H_q][D] of kv_dtype;
  * block_tables: [N][MB] int32 (entries past ceil(ctx/B) are not read);
  * ctx_lens: [N] int32 in [1, min(max_ctx, MB*B)];
  * scale: usually 1/sqrt(D).

@@ -227,7 +227,8 @@ def _workspace(workspace, nbytes, device):
 
 def pa_decode(out, q, pool, block_tables, ctx_lens, max_ctx, scale=None, partition_tokens=0, workspace=None,
               dev_err=None, attend_events=None, stream=None):
-    """Paged decode attention: out [N, H_q, D] (fp32 or the KV dtype)."""
+    """Paged decode attention: out [N, H_q, D] (fp32 or the KV dtype), on the device or in pinned host memory (the
+    kernels then write the rows across the host link: no separate copy of the result)."""
     N, H_q, D = q.shape
     NB, B, _, H_kv, D2 = pool.shape
     MB = block_tables.shape[1]
@@ -239,7 +240,7 @@ def pa_decode(out, q, pool, block_tables, ctx_lens, max_ctx, scale=None, partiti
     nbytes = pa_decode_workspace_bytes(N, H_q, H_kv, D, int(max_ctx), partition_tokens)
     ws = _workspace(workspace, nbytes, q.device)
     L = load()
-    _check(L.pa_decode(_dev(out, "out"), _dtype_code(out.dtype), _dev(q, "q"), _dev(pool, "pool"),
+    _check(L.pa_decode(_acc(out, "out"), _dtype_code(out.dtype), _dev(q, "q"), _dev(pool, "pool"),
                        _dev(block_tables, "block_tables", torch.int32), _dev(ctx_lens, "ctx_lens", torch.int32), N,
                        H_q, H_kv, D, B, MB, NB, int(max_ctx), scale, int(partition_tokens), _dev(ws, "workspace"),
                        ws.numel() * ws.element_size(), _dtype_code(pool.dtype), _err_ptr(dev_err),
@@ -302,7 +303,7 @@ def pa_decode_no_alloc(out, q, pool, block_tables, ctx_lens, max_ctx, scale=None
         raise PAError(PA_ERR_INVALID, "block_tables must be [N, MB] and ctx_lens [N]")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     L = load()
-    _check(L.pa_decode_no_alloc(_dev(out, "out"), _dtype_code(out.dtype), _dev(q, "q"), _dev(pool, "pool"),
+    _check(L.pa_decode_no_alloc(_acc(out, "out"), _dtype_code(out.dtype), _dev(q, "q"), _dev(pool, "pool"),
                                 _dev(block_tables, "block_tables", torch.int32),
                                 _dev(ctx_lens, "ctx_lens", torch.int32), N, H_q, H_kv, D, B, MB, NB, int(max_ctx),
                                 scale, int(partition_tokens), _dtype_code(pool.dtype), _err_ptr(dev_err),

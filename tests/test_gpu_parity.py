@@ -309,6 +309,28 @@ def test_low_precision_output_is_the_rounded_fp32_output(make):
         assert np.all(np.abs(W.bits_to_float(bits, w.dtype) - ref) <= C.ATOL + half_ulp)
 
 
+def test_output_in_pinned_host_memory_equals_device_output():
+    """out may live in pinned host memory: the attention kernel (single-partition rows) and both merge kernels
+    write the rows across the host link, bit for bit what they write into device memory, fp32 and 16-bit."""
+    w = W.llama3_8b(n_seqs=10)
+    c = C.build_paged(w)
+    tab, ctx = c.dev_tables()
+    qd = C.to_dev(c.q, w.dtype)
+    ref = C.oracle_decode(c)
+    for odt in (torch.float32, torch.bfloat16):
+        for pt in (0, -1, 32):
+            dev_out = torch.full((w.N, w.H_q, w.D), float("nan"), dtype=odt, device="cuda")
+            host_out = torch.full((w.N, w.H_q, w.D), float("nan"), dtype=odt).pin_memory()
+            pa.pa_decode(dev_out, qd, c.pool, tab, ctx, int(c.ctx.max()), partition_tokens=pt)
+            pa.pa_decode(host_out, qd, c.pool, tab, ctx, int(c.ctx.max()), partition_tokens=pt)
+            torch.cuda.synchronize()
+            assert torch.equal(dev_out.cpu(), host_out), f"{odt} pt={pt}"
+            if odt == torch.float32:
+                C.assert_close(host_out.numpy(), ref, f"host output pt={pt}")
+    with pytest.raises(pa.PAError):
+        pa.pa_decode(torch.empty((w.N, w.H_q, w.D)), qd, c.pool, tab, ctx, int(c.ctx.max()))  # pageable: refused
+
+
 @pytest.mark.parametrize("R,P,D", [(37, 9, 128), (37, 40, 128), (11, 300, 128), (23, 33, 64)])
 def test_partition_reduce_standalone_matches_oracle_merge(R, P, D):
     """Warp-per-row merge (P < 32) and CTA-per-row merge (P >= 32, rows of up to 300 partitions)."""
