@@ -15,7 +15,8 @@
 //     decreasing length.
 //  2. attend_kernel (persistent, 4 CTAs per SM, 2 warps each): CTA c takes the
 //     whole-partition records c, c + grid, ..., then ragged tails from a shared
-//     counter, longest first.  Warp 1 (producer) streams each record's K/V
+//     counter, longest first; it computes record c from the lengths and streams
+//     it while the schedule is still being written.  Warp 1 (producer) streams each record's K/V
 //     through a ring of shared-memory stages with TMA: one 5-D tensor copy per
 //     KV block brings the block's K and V rows of one head, 128-byte swizzled;
 //     the first stage of a record also carries the record's G query rows.
@@ -43,6 +44,7 @@ namespace pa {
 constexpr int kNumBins = 2048;
 constexpr int kPlanThreads = 1024;
 constexpr int kAttnThreads = 64;
+constexpr int kEarlySeqs = 256;  // sequences a CTA scans for its first record before the schedule is written
 constexpr uint32_t kSwzRowBytes = 128;
 
 enum : int { kFirst = 1, kLast = 2, kDone = 4 };
@@ -284,6 +286,9 @@ struct AttnParams {
     float* part_l;
     float* part_acc;
     int P, PT;
+    // inputs of the schedule, for a CTA that starts on its first record before the schedule is written
+    const int32_t* ctx_lens;
+    int N, H_kv, max_ctx, cap, N_max;
     float scale_log2;
     int nstage;
     int* err;
@@ -334,8 +339,11 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
         if (!PAGED) prefetch_tmap(&tm_b);
     }
     __syncthreads();
-    // everything above overlaps the schedule kernel; from here on its records are needed
-    griddep_wait();
+    // Everything up to the producer's join_schedule() overlaps the schedule kernel.  This kernel is only ever
+    // launched right after the schedule kernel, whose CTAs let it start only once every kernel before them has
+    // finished: from here on the call's inputs (lengths, tables, q, pool) are final, and the outputs and partials
+    // this kernel writes are touched by no earlier kernel still running.  Only the schedule's own output (header,
+    // records) needs the wait.
     griddep_launch_dependents();
 
     const int lane = threadIdx.x & 31;
@@ -344,7 +352,14 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
 
     if (threadIdx.x >= 32) {
         // ------------------------------------------------------------------ producer warp
-        const int total = p.header[0], nwhole = p.header[2];
+        int total = 0, nwhole = 0;
+        bool joined = false;
+        auto join_schedule = [&]() {
+            griddep_wait();
+            total = p.header[0];
+            nwhole = p.header[2];
+            joined = true;
+        };
         const uint64_t pol = policy_evict_first();
         const int bps = kStageTok / Beff;  // boxes per stage
         int slot = 0;
@@ -358,15 +373,52 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
             const int j = i + (int)gridDim.x;
             return j < nwhole ? j : nwhole + atomicAdd(p.header + 1, 1);
         };
-        int nidx = 0;
-        if (lane == 0) nidx = after((int)blockIdx.x - (int)gridDim.x);
-        nidx = __shfl_sync(0xffffffffu, nidx, 0);
-        int4 cur = nidx < total ? p.rec[nidx] : none;
-        if (lane == 0) nidx = after(nidx);
-        nidx = __shfl_sync(0xffffffffu, nidx, 0);
-        int4 nxt = nidx < total ? p.rec[nidx] : none;
-        int pend = 0;
-        if (lane == 0 && nxt.x >= 0) pend = after(nidx);
+        // The CTA's first record, whole partition blockIdx.x of the round robin, follows from the lengths alone
+        // (the schedule orders whole partitions by sequence, partition, kv head): when it lies in the first
+        // kEarlySeqs sequences the CTA streams it before the schedule is written, and joins the schedule for
+        // the records after it.
+        auto early_record = [&]() -> int4 {
+            if (p.PT >= kUnpartitioned) return none;
+            const int j = (int)blockIdx.x / p.H_kv, h = (int)blockIdx.x % p.H_kv;  // whole partition, kv head
+            int c[kEarlySeqs / 32];
+#pragma unroll
+            for (int k = 0; k < kEarlySeqs / 32; ++k) {
+                const int sq = 32 * k + lane;
+                int v = sq < p.N ? p.ctx_lens[sq] : 0;
+                if (v < 1 || v > p.max_ctx || v > p.cap) v = 0;  // as the schedule: no records
+                if (!PAGED && v > 0) {
+                    const int r = p.req_ids[sq];
+                    if (r < 0 || r >= p.N_max) v = 0;
+                }
+                c[k] = v;
+            }
+            int run = 0;  // whole partitions of the sequences before chunk k
+#pragma unroll
+            for (int k = 0; k < kEarlySeqs / 32; ++k) {
+                const int nf = c[k] / p.PT;
+                const int incl = warp_incl_scan(nf);
+                const unsigned hit = __ballot_sync(0xffffffffu, run + incl - nf <= j && j < run + incl);
+                if (hit) {
+                    const int src = __ffs(hit) - 1;
+                    const int first = __shfl_sync(0xffffffffu, run + incl - nf, src);
+                    return make_int4(32 * k + src, h, j - first, __shfl_sync(0xffffffffu, c[k], src));
+                }
+                run += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            return none;
+        };
+        int4 cur = early_record(), nxt = none;
+        int nidx = 0, pend = 0;
+        if (cur.x < 0) {
+            join_schedule();
+            if (lane == 0) nidx = after((int)blockIdx.x - (int)gridDim.x);
+            nidx = __shfl_sync(0xffffffffu, nidx, 0);
+            cur = nidx < total ? p.rec[nidx] : none;
+            if (lane == 0) nidx = after(nidx);
+            nidx = __shfl_sync(0xffffffffu, nidx, 0);
+            nxt = nidx < total ? p.rec[nidx] : none;
+            if (lane == 0 && nxt.x >= 0) pend = after(nidx);
+        }
         // table entries of the first 32 boxes of `it` starting at box `cb`
         auto load_entries = [&](const int4& it, int cb) -> int {
             const int t0 = it.z * p.PT;
@@ -388,7 +440,7 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
                 int ent_nx = 0;
                 if (cb + 32 < nblk)
                     ent_nx = load_entries(cur, cb + 32);
-                else if (nxt.x >= 0)
+                else if (joined && nxt.x >= 0)
                     ent_nx = load_entries(nxt, 0);
                 const int cend = min(cb + 32, nblk);
                 for (int b0 = cb; b0 < cend; b0 += bps, ++st) {
@@ -442,6 +494,15 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
                     }
                 }
                 ent = ent_nx;
+            }
+            if (!joined) {
+                // the early first record is issued: the records after it come from the schedule
+                join_schedule();
+                if (lane == 0) nidx = after((int)blockIdx.x);
+                nidx = __shfl_sync(0xffffffffu, nidx, 0);
+                nxt = nidx < total ? p.rec[nidx] : none;
+                if (lane == 0 && nxt.x >= 0) pend = after(nidx);
+                ent = nxt.x >= 0 ? load_entries(nxt, 0) : 0;
             }
             cur = nxt;
             nidx = __shfl_sync(0xffffffffu, pend, 0);
@@ -956,6 +1017,12 @@ static pa_status run_attend(const DecodeArgs& a, const WorkspaceLayout& L, const
     p.part_acc = L.P > 1 ? reinterpret_cast<float*>(ws + L.part_acc) : nullptr;
     p.P = L.P;
     p.PT = L.PT;
+    p.ctx_lens = a.ctx_lens;
+    p.N = a.N;
+    p.H_kv = a.H_kv;
+    p.max_ctx = a.max_ctx;
+    p.cap = a.paged ? a.MB * a.B : a.S_max;
+    p.N_max = a.N_max;
     p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);  // log2(e)
     p.nstage = nstage;
     p.err = a.dev_err;
