@@ -409,6 +409,14 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
         };
         int4 cur = early_record(), nxt = none;
         int nidx = 0, pend = 0;
+        // joins the schedule after the early first record: the record after it and the one after that
+        auto join_after_first = [&]() {
+            join_schedule();
+            if (lane == 0) nidx = after((int)blockIdx.x);
+            nidx = __shfl_sync(0xffffffffu, nidx, 0);
+            nxt = nidx < total ? p.rec[nidx] : none;
+            if (lane == 0 && nxt.x >= 0) pend = after(nidx);
+        };
         if (cur.x < 0) {
             join_schedule();
             if (lane == 0) nidx = after((int)blockIdx.x - (int)gridDim.x);
@@ -444,6 +452,11 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
                     ent_nx = load_entries(nxt, 0);
                 const int cend = min(cb + 32, nblk);
                 for (int b0 = cb; b0 < cend; b0 += bps, ++st) {
+                    if (!joined && st == nstage) {
+                        // the ring is full of the early record: learn the next one while it drains
+                        join_after_first();
+                        if (cb + 32 >= nblk && nxt.x >= 0) ent_nx = load_entries(nxt, 0);
+                    }
                     if (lane == 0) ok = mbar_wait_bounded(empty_s + 8 * slot, ephase ^ 1, abort_flag);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
@@ -496,12 +509,8 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
                 ent = ent_nx;
             }
             if (!joined) {
-                // the early first record is issued: the records after it come from the schedule
-                join_schedule();
-                if (lane == 0) nidx = after((int)blockIdx.x);
-                nidx = __shfl_sync(0xffffffffu, nidx, 0);
-                nxt = nidx < total ? p.rec[nidx] : none;
-                if (lane == 0 && nxt.x >= 0) pend = after(nidx);
+                // an early first record shorter than the ring: the records after it come from the schedule
+                join_after_first();
                 ent = nxt.x >= 0 ? load_entries(nxt, 0) : 0;
             }
             cur = nxt;
