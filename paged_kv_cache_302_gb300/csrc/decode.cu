@@ -733,26 +733,28 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
                 }
             } else {
                 const size_t r0 = (qrow0 + h0) * p.P + mt.part, r1 = (qrow0 + h1) * p.P + mt.part;
+                // the merge reads the partials right after this kernel: keep them in L2
+                const uint64_t keep = policy_evict_last();
 #pragma unroll
                 for (int i = 0; i < NT; ++i) {
                     const int d = 16 * i + g4;
                     if (h0 < p.G) {
-                        p.part_acc[r0 * D + d] = O[i][0];
-                        p.part_acc[r0 * D + d + 8] = O[i][2];
+                        st_hint(p.part_acc + r0 * D + d, O[i][0], keep);
+                        st_hint(p.part_acc + r0 * D + d + 8, O[i][2], keep);
                     }
                     if (h1 < p.G) {
-                        p.part_acc[r1 * D + d] = O[i][1];
-                        p.part_acc[r1 * D + d + 8] = O[i][3];
+                        st_hint(p.part_acc + r1 * D + d, O[i][1], keep);
+                        st_hint(p.part_acc + r1 * D + d + 8, O[i][3], keep);
                     }
                 }
                 if (g4 == 0) {
                     if (h0 < p.G) {
-                        p.part_m2[r0] = m0;
-                        p.part_l[r0] = L0;
+                        st_hint(p.part_m2 + r0, m0, keep);
+                        st_hint(p.part_l + r0, L0, keep);
                     }
                     if (h1 < p.G) {
-                        p.part_m2[r1] = m1;
-                        p.part_l[r1] = L1;
+                        st_hint(p.part_m2 + r1, m1, keep);
+                        st_hint(p.part_l + r1, L1, keep);
                     }
                 }
             }

@@ -153,6 +153,18 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
     return p;
 }
 
+// L2 keeps lines stored with this policy ahead of others (data read back soon after, by the next kernel).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// fp32 global store with an L2 cache policy.
+__device__ __forceinline__ void st_hint(float* p, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
