@@ -592,9 +592,10 @@ def run_swap(args):
 
 
 def run_prefill(args):
-    """Chunked paged prefill on the tensor cores: Llama-3-8B shapes (32 q / 8 KV heads, D 128, bf16, B 16),
-    16 sequences whose last 2048 of 4096 tokens are the chunk (K/V already in the pool).  FLOPs count the
-    causal score and value products actually needed: 4 * D * (position + 1) per query row and head."""
+    """Chunked paged prefill on the tensor cores: Llama-3-8B shapes (32 q / 8 KV heads, D 128, B 16), 16 sequences
+    whose last 2048 of 4096 tokens are the chunk (K/V already in the pool); bf16, then the same shapes in fp16
+    (whose probabilities need one value product instead of two).  FLOPs count the causal score and value
+    products actually needed: 4 * D * (position + 1) per query row and head."""
     import torch
 
     import paged_kv_cache_302_gb300 as pa
@@ -605,33 +606,36 @@ def run_prefill(args):
     NB = N * nb + 64
     perm = torch.from_numpy(np.random.default_rng(13).permutation(NB)[: N * nb].astype(np.int32))
     tables = perm.view(N, nb).cuda()
-    pool = torch.empty((NB, B, 2, H_kv, D), dtype=torch.bfloat16, device="cuda").normal_()
     ctx = torch.full((N,), ctx_len, dtype=torch.int32, device="cuda")
     q_start = torch.arange(0, (N + 1) * chunk, chunk, dtype=torch.int32, device="cuda")
-    q = torch.empty((N * chunk, H_q, D), dtype=torch.bfloat16, device="cuda").normal_()
     out = torch.empty((N * chunk, H_q, D), dtype=torch.float32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     pos = np.arange(ctx_len - chunk, ctx_len, dtype=np.float64)
     flops = N * H_q * 4.0 * D * float((pos + 1).sum())
-    for _ in range(args.warmup):
-        pa.pa_prefill(out, q, pool, tables, ctx, q_start, chunk, dev_err=err)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        pa.pa_prefill(out, q, pool, tables, ctx, q_start, chunk, dev_err=err)
-    e1.record()
-    torch.cuda.synchronize()
-    assert int(err.item()) == 0
-    t = e0.elapsed_time(e1) * 1e-3 / args.steps
     peak = 1900.0
     try:
         peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"])
     except Exception:
         pass
-    tf = flops / t / 1e12
-    print(json.dumps({"measure": "pa_prefill", "unit": "TFLOP/s", "value": tf, "ms_per_call": t * 1e3,
-                      "peak_bf16_tflops": peak, "frac": tf / peak, "seqs": N, "ctx": ctx_len, "chunk": chunk,
-                      "flops_per_call": flops, "steps": args.steps}), flush=True)
+    for dt, name in ((torch.bfloat16, "bf16"), (torch.float16, "f16")):
+        pool = torch.empty((NB, B, 2, H_kv, D), dtype=dt, device="cuda").normal_()
+        q = torch.empty((N * chunk, H_q, D), dtype=dt, device="cuda").normal_()
+        for _ in range(args.warmup):
+            pa.pa_prefill(out, q, pool, tables, ctx, q_start, chunk, dev_err=err)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            pa.pa_prefill(out, q, pool, tables, ctx, q_start, chunk, dev_err=err)
+        e1.record()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        t = e0.elapsed_time(e1) * 1e-3 / args.steps
+        tf = flops / t / 1e12
+        # the fp16 dense tensor rate equals the bf16 one on this GPU
+        print(json.dumps({"measure": "pa_prefill", "kv_dtype": name, "unit": "TFLOP/s", "value": tf,
+                          "ms_per_call": t * 1e3, "peak_bf16_tflops": peak, "frac": tf / peak, "seqs": N,
+                          "ctx": ctx_len, "chunk": chunk, "flops_per_call": flops, "steps": args.steps}), flush=True)
+        del pool, q
     return 0
 
 

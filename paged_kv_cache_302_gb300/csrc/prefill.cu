@@ -14,13 +14,13 @@
 //     the copies of the tile's b-th KV block;
 //   * warp 9 (MMA, one thread): S_w = Q_w K^T as tcgen05.mma (M 128, N 128,
 //     K 16 steps) into TMEM columns [128w, 128w + 128), and O_w += P_hi V +
-//     P_lo V with P read from those same TMEM columns (the A operand) and V an
+//     P_lo V (bf16; fp16 needs only P V) with P read from those same TMEM columns (the A operand) and V an
 //     MN-major shared-memory operand; O_w sits in TMEM columns 256 + D w;
 //   * warps 0-3 and 4-7 (softmax, one warpgroup per query tile): every thread
 //     owns one TMEM lane = one query row; it reads its S row with tcgen05.ld,
 //     masks causally, keeps the running maximum (rescaling O only when the
 //     maximum grows by more than 2^8), and writes the probabilities back over S
-//     as a high and a low 16-bit part (tcgen05.st).
+//     as a high and a low 16-bit part for bf16, one fp16 part for fp16 (tcgen05.st).
 // Hand-offs are mbarriers; every wait is bounded.  Finally every thread reads
 // its O row, divides by its exponential sum and stores the row.
 #include <cuda.h>
@@ -203,6 +203,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     constexpr int NT = kPfKeys / 16;    // k-steps of O += P V
     constexpr int NS = kPfStages;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    // bf16 P (8-bit significand) would put the relative L2 error near 1e-3, so bf16 keeps P as a high and a low
+    // part (two value products); fp16 P (11 bits, ~1.4e-4) needs only the one
+    constexpr bool kSplitP = kBf16;
     constexpr uint32_t idesc_s = umma_idesc(kBf16, kPfRows, kPfKeys, false);
     constexpr uint32_t idesc_o = umma_idesc(kBf16, kPfRows, D, true);
     constexpr uint32_t kTile = DH * kRegion;  // one Q tile (128 rows x D), or one K or V tile (128 keys x D)
@@ -347,7 +350,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             umma_commit(sfull0 + 8 * w);
             if (w == 1) umma_commit(kfree0 + 8 * st(j));  // K_j has served both query tiles
         };
-        auto issue_pv = [&](int w, int j) {  // O_w += P_hi V + P_lo V, P read from TMEM
+        auto issue_pv = [&](int w, int j) {  // O_w += P_hi V (+ P_lo V for bf16), P read from TMEM
             const uint32_t vb = sV0 + st(j) * kTile;
             const uint32_t pcol = tmem + (uint32_t)w * kPfKeys;
             const uint32_t ocol = tmem + 2 * kPfKeys + (uint32_t)w * D;
@@ -357,7 +360,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             for (int ks = 0; ks < NT; ++ks) {
                 const uint64_t vdesc = dv + (uint64_t)(ks * vstep);
                 umma_f16_ta(ocol, pcol + ks * 8, vdesc, idesc_o, (j > 0 || ks > 0));
-                umma_f16_ta(ocol, pcol + kPfKeys / 2 + ks * 8, vdesc, idesc_o, 1u);
+                if (kSplitP) umma_f16_ta(ocol, pcol + kPfKeys / 2 + ks * 8, vdesc, idesc_o, 1u);
             }
             umma_commit(pvd0 + 8 * w);
             if (w == 1) umma_commit(vfree0 + 8 * st(j));
@@ -459,11 +462,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                     x.y = fast_exp2(x.y);
                     ls[(i >> 1) & 1] = fadd2(ls[(i >> 1) & 1], x);
                     hi[i / 2] = Mma<T>::pack(x.x, x.y);
-                    const float2 f = fsub2(x, Mma<T>::unpack(hi[i / 2]));
-                    lo[i / 2] = Mma<T>::pack(f.x, f.y);
+                    if (kSplitP) {
+                        const float2 f = fsub2(x, Mma<T>::unpack(hi[i / 2]));
+                        lo[i / 2] = Mma<T>::pack(f.x, f.y);
+                    }
                 }
                 tmem_st16(t_s + c * 16, hi);
-                tmem_st16(t_s + kPfKeys / 2 + c * 16, lo);
+                if (kSplitP) tmem_st16(t_s + kPfKeys / 2 + c * 16, lo);
             }
             const float2 lsum = fadd2(ls[0], ls[1]);
             l = fmaf(l, alpha, lsum.x + lsum.y);
