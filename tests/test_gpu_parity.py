@@ -246,6 +246,36 @@ def test_schedule_covers_every_work_item_once_longest_first(N, H_kv, pt, max_len
     C.assert_close(got[pairs[:, 0], pairs[:, 1]], ref[pairs[:, 0], pairs[:, 1]], f"schedule N={N}")
 
 
+def test_decode_right_after_a_cache_write_reads_the_new_token():
+    """A decode launched right after the cache write on the same stream, with no synchronisation between them,
+    reads the token the write just stored, also where that token completes a whole 512-token partition (the
+    attention kernel streams its first whole partition while the schedule is still being written).  The new
+    token's key is aligned with its queries, so it dominates every row's softmax: a stale read would show."""
+    rng = np.random.default_rng(31)
+    N, B = 48, 16
+    ctx = rng.choice([512, 1024, 1536, 2048, 700, 1500], size=N).astype(np.int32)
+    ctx[:6] = [512, 1024, 1536, 2048, 2560, 3072]
+    NB = int(((ctx + B - 1) // B).sum()) + 16
+    w = W.Workload("after_write", 31, N, 32, 8, 128, B, "bf16", ctx, NB, rng.permutation(NB).astype(np.int32))
+    c = C.build_paged(w, check_pool=False)
+    tab, ctx = c.dev_tables()
+    last = c.ctx - 1
+    slots = (c.tables[np.arange(w.N), last // w.B].astype(np.int64) * w.B + last % w.B)
+    q = W.bits_to_float(c.q, w.dtype).reshape(w.N, w.H_kv, w.G, w.D)
+    for it in range(4):
+        k_new = W.round_bits(4.0 * q[:, :, it % w.G, :], w.dtype)                     # [N, H_kv, D]
+        v_new = W.normal_bits(rng, (w.N, w.H_kv, w.D), w.dtype)
+        oracle.reshape_and_cache(k_new, v_new, c.host_pool, slots)
+        qd = C.to_dev(c.q, w.dtype)
+        kd, vd, sd = C.to_dev(k_new, w.dtype), C.to_dev(v_new, w.dtype), torch.from_numpy(slots).cuda()
+        out = torch.full((w.N, w.H_q, w.D), float("nan"), device="cuda")
+        torch.cuda.synchronize()
+        pa.pa_reshape_and_cache(kd, vd, c.pool, sd)
+        pa.pa_decode(out, qd, c.pool, tab, ctx, int(c.ctx.max()))
+        torch.cuda.synchronize()
+        C.assert_close(out.cpu().numpy(), C.oracle_decode(c), f"decode after write, round {it}")
+
+
 def test_block_relabelling_gives_identical_bits():
     w = W.llama3_8b(n_seqs=12)
     c = C.build_paged(w, check_pool=False)
