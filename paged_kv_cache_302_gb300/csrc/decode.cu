@@ -16,20 +16,22 @@
 //  2. attend_kernel (persistent, 4 CTAs per SM, 2 warps each): CTA c takes the
 //     whole-partition records c, c + grid, ..., then ragged tails from a shared
 //     counter, longest first; it computes record c from the lengths and streams
-//     it while the schedule is still being written.  Warp 1 (producer) streams each record's K/V
-//     through a ring of shared-memory stages with TMA: one 5-D tensor copy per
-//     KV block brings the block's K and V rows of one head, 128-byte swizzled;
+//     it while the schedule is still being written.  Warp 1 (producer) streams
+//     each record's K/V through a ring of shared-memory stages with TMA: one
+//     5-D tensor copy per KV block brings the block's K and V rows of one head,
+//     128-byte swizzled;
 //     the first stage of a record also carries the record's G query rows.
 //     Warp 0 (consumer) computes S^T = K Q^T and O^T += V^T P^T with
 //     mma.sync m16n8k16 (tokens on M, the <= 8 query heads of the KV head on N),
 //     an online softmax in base 2 between stages, and writes the normalised
-//     output, or the partition's (m2, l, acc) when the context has several.
+//     output, or the partition's (m2, l, acc) when the context has several
+//     (stored with an L2 evict_last policy for the merge).
 //  3. partition_reduce_kernel (one warp per row; partition_reduce_wide_kernel,
 //     one CTA per row, from 32 partitions per row): merges the partials of
 //     multi-partition rows.
 // Each kernel is launched with programmatic stream serialisation, so its CTAs
 // start while the previous kernel drains and wait (griddepcontrol.wait)
-// before touching memory.
+// before touching memory the previous kernel writes.
 #include <cuda.h>
 
 #include <algorithm>
