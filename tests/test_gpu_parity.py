@@ -276,6 +276,99 @@ def test_decode_right_after_a_cache_write_reads_the_new_token():
         C.assert_close(out.cpu().numpy(), C.oracle_decode(c), f"decode after write, round {it}")
 
 
+_GUARD = 4096  # bytes of sentinel before and after a carved buffer (keeps 32-byte alignment)
+
+
+def _carved(shape, dtype):
+    """(backing buffer, tensor of `shape`) with the tensor carved out of the middle of a device buffer whose
+    first and last _GUARD bytes hold the sentinel 0x5A."""
+    n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    big = torch.full((2 * _GUARD + n,), 0x5A, dtype=torch.uint8, device="cuda")
+    return big, big[_GUARD: _GUARD + n].view(dtype).view(shape)
+
+
+def _margins_intact(*bigs):
+    torch.cuda.synchronize()
+    for big in bigs:
+        edge = torch.cat([big[:_GUARD], big[-_GUARD:]])
+        assert bool((edge == 0x5A).all()), "a kernel wrote outside its buffer"
+
+
+def test_no_call_writes_outside_its_buffers():
+    """Every device buffer of the tiny worked example (pool, slots, tables, query, output, workspace, copy pairs,
+    table updates) and of a small prefill is carved out of a larger allocation with sentinel margins; after
+    cache writes, block copies, table updates, decodes in all partition modes and a prefill, the margins are
+    unchanged, and the results still match the oracle."""
+    w = W.tiny()
+    alloc = pa.BlockAllocator(w.NB, w.B, w.free_order)
+    slots = []
+    for sq in range(w.N):
+        alloc.add_seq(sq)
+        slots.append(alloc.append_slots(sq, int(w.ctx[sq]))[0])
+    slots = np.concatenate(slots)
+    tables, ctx = alloc.block_tables(list(range(w.N)), w.max_blocks_per_seq())
+    k, v = W.token_kv(w, slots.size)
+    shape = (w.NB, w.B, 2, w.H_kv, w.D)
+    pool_big, pool = _carved(shape, torch.float16)
+    pool.view(torch.int16).fill_(C.nan16(w.dtype))
+    host = np.full(shape, W.NAN_BITS[w.dtype], dtype=np.uint16)
+    bigs = [pool_big]
+
+    def dev(a, dtype):
+        big, t = _carved(a.shape, dtype)
+        t.copy_(torch.from_numpy(np.ascontiguousarray(a)).view(dtype) if dtype in (torch.float16, torch.bfloat16)
+                else torch.from_numpy(np.ascontiguousarray(a)))
+        bigs.append(big)
+        return t
+
+    kd, vd = dev(k.view(np.int16), torch.float16), dev(v.view(np.int16), torch.float16)
+    pa.pa_reshape_and_cache(kd, vd, pool, dev(slots, torch.int64))
+    oracle.reshape_and_cache(k, v, host, slots)
+    free = sorted(set(range(w.NB)) - set(tables[tables >= 0].tolist()))
+    pairs = np.array([[tables[3][0], free[0]], [tables[2][1], free[1]]], dtype=np.int64)
+    pa.pa_copy_blocks(pool, dev(pairs, torch.int64))
+    oracle.copy_blocks(host, pairs)
+    _margins_intact(*bigs)
+    assert np.array_equal(C.to_bits(pool), host)
+    tab, ctx_d = dev(tables, torch.int32), dev(ctx.astype(np.int32), torch.int32)
+    q = W.queries(w)
+    qd = dev(q.view(np.int16), torch.float16)
+    ref = oracle.paged_decode(q, host, tables, ctx, w.dtype)
+    for pt in (0, -1, 32):
+        out_big, out = _carved((w.N, w.H_q, w.D), torch.float32)
+        ws_big, ws = _carved((pa.pa_decode_workspace_bytes(w.N, w.H_q, w.H_kv, w.D, int(ctx.max()), pt),), torch.uint8)
+        ws.fill_(0xAB)
+        pa.pa_decode(out, qd, pool, tab, ctx_d, int(ctx.max()), partition_tokens=pt, workspace=ws)
+        _margins_intact(out_big, ws_big, *bigs)
+        C.assert_close(out.cpu().numpy(), ref, f"guarded decode pt={pt}")
+    upd = np.array([[0, 1, free[2]], [3, 2, free[3]], [-1, 0, 0]], dtype=np.int32)
+    pa.pa_update_block_tables(tab, dev(upd, torch.int32))
+    _margins_intact(*bigs)
+    want = tables.copy()
+    want[0, 1], want[3, 2] = free[2], free[3]
+    assert np.array_equal(tab.cpu().numpy(), want)
+
+    # prefill (blocks of 16 tokens): chunks of the last 40 and 100 tokens of two short sequences
+    ctx_p = np.array([300, 130], dtype=np.int32)
+    NBp = int(((ctx_p + 15) // 16).sum()) + 8
+    wp = W.Workload("guard_prefill", 4, 2, 32, 8, 128, 16, "bf16", ctx_p, NBp,
+                    np.random.default_rng(4).permutation(NBp).astype(np.int32))
+    cp = C.build_paged(wp)
+    chunks = [40, 100]
+    q_start = np.array([0, 40, 140], dtype=np.int32)
+    qp = W.normal_bits(np.random.default_rng(4), (140, wp.H_q, wp.D), wp.dtype)
+    out_big, outp = _carved((140, wp.H_q, wp.D), torch.float32)
+    pt_tab, pt_ctx = cp.dev_tables()
+    qs_big, qs_d = _carved((3,), torch.int32)
+    qs_d.copy_(torch.from_numpy(q_start))
+    q_big, q_d = _carved(qp.shape, torch.bfloat16)
+    q_d.copy_(torch.from_numpy(qp.view(np.int16)).view(torch.bfloat16))
+    pa.pa_prefill(outp, q_d, cp.pool, pt_tab, pt_ctx, qs_d, max(chunks))
+    _margins_intact(out_big, qs_big, q_big)
+    refp = oracle.paged_prefill(qp, cp.host_pool, cp.tables, cp.ctx, q_start, wp.dtype, nthreads=0)
+    C.assert_close(outp.cpu().numpy(), refp, "guarded prefill")
+
+
 def test_block_relabelling_gives_identical_bits():
     w = W.llama3_8b(n_seqs=12)
     c = C.build_paged(w, check_pool=False)
