@@ -68,6 +68,16 @@ const char* pa_version(void);
 /* Number of kernels this library has launched in this process (all threads). */
 uint64_t pa_launch_count(void);
 
+/* Time limit, in nanoseconds, of every wait inside the kernels launched from
+ * now on by any thread (the watchdog of "no kernel waits without a time
+ * limit" above); 0 restores the built-in 1 s.  A wait that runs out sets
+ * PA_DEV_ERR_TIMEOUT and the kernel returns, leaving that call's outputs
+ * undefined; before returning it still waits, with the built-in limit, for
+ * the copies and tensor-core products it has issued, so the next call finds
+ * the GPU and the caller's buffers usable.  A very short limit makes the
+ * waits run out on purpose, which is how the timeout exit is tested. */
+void pa_set_wait_limit_ns(uint64_t ns);
+
 /* ------------------------------------------------------------------------
  * Cache write ([PA] 技術的詳細 / PagedAttentionアルゴリズム: tokens are stored in
  * fixed-size blocks reached through the block table; the slot encoding

@@ -66,6 +66,7 @@ def _declare(L):
         "pa_last_error": ([], ctypes.c_char_p),
         "pa_version": ([], ctypes.c_char_p),
         "pa_launch_count": ([], u64),
+        "pa_set_wait_limit_ns": ([u64], None),
         "pa_reshape_and_cache": ([P, P, P, P, i32, i32, i32, i32, i32, i32, P, P], i32),
         "pa_copy_blocks": ([P, P, i32, i32, i32, i32, i32, i32, P, P], i32),
         "pa_decode_workspace_bytes": ([i32, i32, i32, i32, i32, i32], sz),
@@ -133,6 +134,11 @@ def version() -> str:
 
 def launch_count() -> int:
     return int(load().pa_launch_count())
+
+
+def pa_set_wait_limit_ns(ns: int):
+    """Time limit of the in-kernel waits of later launches (0: the built-in 1 s)."""
+    load().pa_set_wait_limit_ns(int(ns))
 
 
 # ----------------------------------------------------------------------------- marshalling helpers

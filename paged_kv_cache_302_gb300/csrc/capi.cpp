@@ -28,6 +28,13 @@ pa_status cuda_fail(cudaError_t e, const char* what) {
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+static std::atomic<uint64_t> g_wait_ns{0};  // 0: the built-in limit
+
+uint64_t wait_limit_ns() {
+    const uint64_t ns = g_wait_ns.load(std::memory_order_relaxed);
+    return ns ? ns : 1000000000ull;
+}
+
 // NVTX ranges around every device call, for profiler timelines; off unless PA_NVTX is set to a non-zero value
 // (read once), so a call costs one predictable branch when they are off.
 static bool nvtx_enabled() {
@@ -92,6 +99,8 @@ const char* pa_last_error(void) { return g_msg; }
 const char* pa_version(void) { return "pa 0.1.0 (sm_103a)"; }
 
 uint64_t pa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void pa_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns, std::memory_order_relaxed); }
 
 pa_status pa_reshape_and_cache(const void* k, const void* v, void* pool, const int64_t* slot_mapping, int T, int NB,
                                int B, int H_kv, int D, pa_dtype dtype, int* dev_err, void* stream) {

@@ -293,6 +293,7 @@ struct AttnParams {
     int N, H_kv, max_ctx, cap, N_max;
     float scale_log2;
     int nstage;
+    uint64_t wait_ns;  // limit of the ring waits (the exit path waits with kWaitLimitNs)
     int* err;
 };
 
@@ -366,6 +367,7 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
         const int bps = kStageTok / Beff;  // boxes per stage
         int slot = 0;
         uint32_t ephase = 0;
+        int narm = 0;  // stages armed so far (stage i's k-th arm completes phase k of full_bar[i])
         bool ok = true;
         const int4 none = make_int4(-1, 0, 0, 0);
         // record order: the whole partitions round robin (CTA c takes c, c + grid, ... below nwhole), then the
@@ -459,9 +461,10 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
                         join_after_first();
                         if (cb + 32 >= nblk && nxt.x >= 0) ent_nx = load_entries(nxt, 0);
                     }
-                    if (lane == 0) ok = mbar_wait_bounded(empty_s + 8 * slot, ephase ^ 1, abort_flag);
+                    if (lane == 0) ok = mbar_wait_bounded(empty_s + 8 * slot, ephase ^ 1, abort_flag, p.wait_ns);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
+                    ++narm;  // armed below: expect_tx and every copy of the stage, with no wait in between
                     const int tok0 = st * kStageTok;
                     const int nvalid = min(kStageTok, ntok - tok0);
                     const int nb = min(bps, nblk - b0);
@@ -521,18 +524,29 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
             if (lane == 0 && nxt.x >= 0) pend = after(nidx);
         }
         if (ok && lane == 0) {
-            ok = mbar_wait_bounded(empty_s + 8 * slot, ephase ^ 1, abort_flag);
+            ok = mbar_wait_bounded(empty_s + 8 * slot, ephase ^ 1, abort_flag, p.wait_ns);
             if (ok) {
                 meta[slot].flags = kDone;
                 mbar_arrive(full_s + 8 * slot);
+                ++narm;
             }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok && lane == 0) {
-            flag_error(p.err, PA_DEV_ERR_TIMEOUT);
-            *abort_flag = 1;
-            // let copies already issued land before the CTA exits
-            for (int i = 0; i < nstage; ++i) mbar_wait_bounded(full_s + 8 * i, 0, nullptr, 1000000ull);
+        if (lane == 0) {
+            if (!ok) {
+                flag_error(p.err, PA_DEV_ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // Copies land in this CTA's shared memory, so it may not exit while one is in flight.  When the
+            // consumer gave up (a wait ran out, or it saw the abort flag), stages it never reached can still be
+            // landing, whether or not this warp itself ran into a wait.  Stage i's last arm is arm
+            // i + m * nstage, m = (narm - 1 - i) / nstage, and it completes phase m of full_bar[i]; waiting on
+            // that phase's parity covers every earlier arm too (each was consumed before the next was armed).
+            // In a call that ran to completion every such phase is already complete.
+            for (int i = 0; i < nstage && i < narm; ++i) {
+                const int m = (narm - 1 - i) / nstage;
+                mbar_wait_bounded(full_s + 8 * i, (uint32_t)(m & 1), nullptr, kWaitLimitNs);
+            }
         }
         return;
     }
@@ -568,7 +582,7 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
     uint32_t fphase = 0;
     const float NEG_INF = -INFINITY;
     while (true) {
-        if (!mbar_wait_bounded(full_s + 8 * slot, fphase, abort_flag)) {
+        if (!mbar_wait_bounded(full_s + 8 * slot, fphase, abort_flag, p.wait_ns)) {
             if (lane == 0) {
                 flag_error(p.err, PA_DEV_ERR_TIMEOUT);
                 *abort_flag = 1;
@@ -1038,6 +1052,7 @@ static pa_status run_attend(const DecodeArgs& a, const WorkspaceLayout& L, const
     p.N_max = a.N_max;
     p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);  // log2(e)
     p.nstage = nstage;
+    p.wait_ns = wait_limit_ns();
     p.err = a.dev_err;
 
     if (a.attend_events && a.attend_events[0]) {

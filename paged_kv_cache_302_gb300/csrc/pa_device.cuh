@@ -24,8 +24,11 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-// A wait gives up after this many nanoseconds (the kernel then flags
-// PA_DEV_ERR_TIMEOUT and returns).  Legitimate waits last microseconds.
+// A wait gives up after this many nanoseconds unless pa_set_wait_limit_ns names
+// another limit (the kernel then flags PA_DEV_ERR_TIMEOUT and returns).
+// Legitimate waits last microseconds.  The waits of an exit path, which let
+// copies and tensor-core products already issued land before shared memory or
+// TMEM is released, always use this limit.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 // ----------------------------------------------------------------------------- programmatic dependent launch

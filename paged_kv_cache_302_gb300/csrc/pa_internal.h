@@ -14,6 +14,8 @@ pa_status fail(pa_status st, const char* fmt, ...);
 // Maps a CUDA error to PA_ERR_CUDA with the call site in the message.
 pa_status cuda_fail(cudaError_t e, const char* what);
 void count_launch();
+// Limit of the main in-kernel waits for launches made now (pa_set_wait_limit_ns; default 1 s).
+uint64_t wait_limit_ns();
 
 // ----------------------------------------------------------------------------- cache ops
 

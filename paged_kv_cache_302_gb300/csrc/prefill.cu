@@ -50,6 +50,7 @@ struct PrefillParams {
     void* out;
     int out_dtype;
     float scale_log2;
+    uint64_t wait_ns;  // limit of the hand-off waits (the exit path waits with kWaitLimitNs)
     int* err;
 };
 
@@ -180,17 +181,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-// Barrier 1 over the softmax warpgroups; returns the AND of `pred` over them.
-__device__ __forceinline__ bool softmax_bar_and(bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "n"(kPfSoftmaxThreads)
-        : "memory");
-    return r != 0;
-}
-
 // ----------------------------------------------------------------------------- kernel
 
 template <typename T, int D>
@@ -214,12 +204,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     const uint32_t sb = smem_addr(base);
     // Q[2] | K[NS] | V[NS] | barriers
     const uint32_t sQ0 = sb, sK0 = sQ0 + 2 * kTile, sV0 = sK0 + NS * kTile, sBar = sV0 + NS * kTile;
-    // barriers: q; k_full, v_full, k_free, v_free [NS]; s_full, pv_done, p_ready [2] (one per query tile)
+    // barriers: q; k_full, v_full, k_free, v_free [NS]; s_full, pv_done, p_ready [2] (one per query tile);
+    // mma_done (the MMA thread's last commit: every product it issued has completed)
     const uint32_t qbar = sBar, kfull0 = qbar + 8, vfull0 = kfull0 + 8 * NS, kfree0 = vfull0 + 8 * NS,
-                   vfree0 = kfree0 + 8 * NS, sfull0 = vfree0 + 8 * NS, pvd0 = sfull0 + 16, prd0 = pvd0 + 16;
-    constexpr int kBars = 1 + 4 * NS + 6;
+                   vfree0 = kfree0 + 8 * NS, sfull0 = vfree0 + 8 * NS, pvd0 = sfull0 + 16, prd0 = pvd0 + 16,
+                   mmadone = prd0 + 16;
+    constexpr int kBars = 1 + 4 * NS + 6 + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + (sBar - sb) + 8 * kBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + (sBar - sb) + 8 * kBars + 4);
+    // K and V tiles whose copies the TMA warp has issued (tile t uses stage t % NS), kept in shared memory for
+    // the exit path rather than in registers
+    volatile int* armed = abort_flag + 1;
 
     griddep_wait();
     griddep_launch_dependents();
@@ -258,6 +253,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         mbar_init(prd0, kPfRows);
         mbar_init(prd0 + 8, kPfRows);
         *abort_flag = 0;
+        armed[0] = armed[1] = 0;
         fence_mbar_init();
     }
     // rows past TQ*G (when G does not divide 128) are never loaded: clear them once in both query tiles
@@ -275,7 +271,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;  // columns: S/P of query tile w at 128 w, O_w at 256 + D w
     auto waited = [&](uint32_t bar, uint32_t parity) {
-        const bool w = mbar_wait_bounded(bar, parity, abort_flag);
+        const bool w = mbar_wait_bounded(bar, parity, abort_flag, p.wait_ns);
         if (!w) *abort_flag = 1;
         return w;
     };
@@ -316,7 +312,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                 if (!ok) break;
                 const uint32_t bar = (which ? vfull0 : kfull0) + 8 * b;
                 const uint32_t dst = (which ? sV0 : sK0) + b * kTile;
-                if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+                if (lane == 0) {
+                    armed[which] = t + 1;  // expect_tx and every copy below, with no wait in between
+                    mbar_arrive_expect_tx(bar, bytes);
+                }
                 __syncwarp();
                 if (lane < nblk) {
                     if (which ? v_blk : k_blk)
@@ -387,6 +386,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                     }
                 }
             }
+            // arrives once every product issued above has completed (at once when none was issued)
+            umma_commit(mmadone);
         }
         __syncwarp();
     } else {
@@ -539,14 +540,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             }
         }
     }
+    // Nothing issued may still be running when TMEM and shared memory are released: the tensor-core products
+    // (the MMA thread's last commit) and the copies (the last arm of every stage: stage b's arms are tiles
+    // b, b + NS, ...; each was consumed before the next was armed, so only the last can be in flight).  After a
+    // wait ran out these can be anywhere; in a call that ran to completion they have all landed.
+    if (warp == 9 && lane == 0) mbar_wait_bounded(mmadone, 0, nullptr);
+    if (warp == 8 && lane == 0) {
+        mbar_wait_bounded(qbar, 0, nullptr);
+        for (int which = 0; which < 2; ++which) {
+            const int n = armed[which];
+            for (int b = 0; b < NS && b < n; ++b)
+                mbar_wait_bounded((which ? vfull0 : kfull0) + 8 * b, ph(b + (n - 1 - b) / NS * NS), nullptr);
+        }
+    }
     tc_fence_before();
     ok = __syncthreads_and(ok && !*abort_flag);
-    if (!ok) {
-        if (tid == 0) flag_error(p.err, PA_DEV_ERR_TIMEOUT);
-        // let issued tensor-core and copy work land before the memory it uses is released
-        if (tid == 0) mbar_wait_bounded(pvd0 + 8, (uint32_t)((ntiles - 1) & 1), nullptr, 1000000ull);
-        __syncthreads();
-    }
+    if (!ok && tid == 0) flag_error(p.err, PA_DEV_ERR_TIMEOUT);
     if (warp == 0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
@@ -601,6 +610,7 @@ static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const 
     p.out = a.out;
     p.out_dtype = a.out_dtype;
     p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
+    p.wait_ns = wait_limit_ns();
     p.err = a.dev_err;
     const dim3 grid((a.max_q_len + 2 * p.TQ - 1) / (2 * p.TQ), a.H_kv, a.N);
     e = launch_kernel(kern, grid, dim3(kPfThreads), smem, a.stream, tq, tkv, tkv_blk, p);
