@@ -9,6 +9,16 @@
 
 namespace pa {
 
+// Grid of a per-token copy: one CTA per token up to 16 resident CTAs per SM of the current device.
+static int token_grid(int T) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || sms < 1)
+        sms = 1;
+    const long cap = 16L * sms;
+    return T < cap ? T : (int)cap;
+}
+
 // One CTA per token (grid-stride).  Token i's K row and V row (H_kv*D elements
 // each, contiguous in both source and pool) are copied to slot slots[i].
 __global__ void __launch_bounds__(128) reshape_and_cache_kernel(const uint4* __restrict__ k,
@@ -42,12 +52,45 @@ pa_status launch_reshape_and_cache(const void* k, const void* v, void* pool, con
                                    int NB, int B, int H_kv, int D, int* dev_err, cudaStream_t stream) {
     if (T == 0) return PA_OK;
     const int row_vec = H_kv * D * 2 / 16;
-    int grid = T < 152 * 16 ? T : 152 * 16;
+    const int grid = token_grid(T);
     cudaError_t e = launch_kernel(reshape_and_cache_kernel, dim3(grid), dim3(128), 0, stream,
                                   static_cast<const uint4*>(k), static_cast<const uint4*>(v),
                                   static_cast<uint4*>(pool), slot_mapping, T, (int64_t)NB * B, row_vec, B, dev_err);
     count_launch();
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "reshape_and_cache launch");
+}
+
+// Chained pairs (a destination that is also a source, or a destination named twice) make the result of a copy
+// call depend on the order of the copies; they are flagged, in one pass over the pairs.  CTA r owns the block ids
+// [r * kCheckIds, (r + 1) * kCheckIds): it marks the destinations that fall in its range in a shared-memory bitmap
+// (a bit found already set is a repeated destination), then looks up the sources in its range.  One CTA covers
+// 262144 block ids, so a pool of up to that many blocks is checked by a single CTA reading every pair twice.
+constexpr int kCheckThreads = 1024;
+constexpr int kCheckWords = 8192;  // 32 KB of bitmap
+constexpr int64_t kCheckIds = (int64_t)kCheckWords * 32;
+
+__global__ void __launch_bounds__(kCheckThreads) check_pairs_kernel(const int64_t* __restrict__ pairs, int n,
+                                                                    int* err) {
+    griddep_wait();
+    griddep_launch_dependents();
+    __shared__ uint32_t bits[kCheckWords];
+    const int64_t lo = (int64_t)blockIdx.x * kCheckIds;
+    for (int i = threadIdx.x; i < kCheckWords; i += blockDim.x) bits[i] = 0;
+    __syncthreads();
+    bool bad = false;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int64_t d = pairs[2 * i + 1] - lo;
+        if (d >= 0 && d < kCheckIds) {
+            const uint32_t m = 1u << (d & 31);
+            if (atomicOr(&bits[d >> 5], m) & m) bad = true;
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int64_t s = pairs[2 * i] - lo;
+        if (s >= 0 && s < kCheckIds && (bits[s >> 5] >> (s & 31)) & 1u) bad = true;
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0) flag_error(err, PA_DEV_ERR_BLOCK);
 }
 
 // grid.x = pair index, grid.y = chunk of the block; each thread moves
@@ -56,7 +99,7 @@ constexpr int kCopyThreads = 256;
 constexpr int kCopyUnroll = 4;
 
 __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(uint4* __restrict__ pool,
-                                                                   const int64_t* __restrict__ pairs, int n, int NB,
+                                                                   const int64_t* __restrict__ pairs, int NB,
                                                                    int64_t blk_vec, int* err) {
     griddep_wait();
     griddep_launch_dependents();
@@ -65,14 +108,6 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(uint4* __rest
     if (src < 0 || src >= NB || dst < 0 || dst >= NB) {
         if (threadIdx.x == 0 && blockIdx.y == 0) flag_error(err, PA_DEV_ERR_BLOCK);
         return;
-    }
-    if (blockIdx.y == 0) {
-        // chained pairs (a destination that is also a source, or a repeated
-        // destination) make the result order dependent: flag them
-        for (int j = threadIdx.x; j < n; j += blockDim.x) {
-            const int64_t sj = pairs[2 * j], dj = pairs[2 * j + 1];
-            if (sj == dst || (j != i && dj == dst)) flag_error(err, PA_DEV_ERR_BLOCK);
-        }
     }
     const uint4* s = pool + src * blk_vec;
     uint4* d = pool + dst * blk_vec;
@@ -99,9 +134,12 @@ pa_status launch_copy_blocks(void* pool, const int64_t* pairs, int n, int NB, in
     const int64_t chunk = (int64_t)kCopyThreads * kCopyUnroll;
     int64_t gy = (blk_vec + chunk - 1) / chunk;
     if (gy > 65535) gy = 65535;
-    dim3 grid(n, (unsigned)gy);
-    cudaError_t e = launch_kernel(copy_blocks_kernel, grid, dim3(kCopyThreads), 0, stream, static_cast<uint4*>(pool),
-                                  pairs, n, NB, blk_vec, dev_err);
+    cudaError_t e = launch_kernel(check_pairs_kernel, dim3((unsigned)(((int64_t)NB + kCheckIds - 1) / kCheckIds)),
+                                  dim3(kCheckThreads), 0, stream, pairs, n, dev_err);
+    count_launch();
+    if (e != cudaSuccess) return cuda_fail(e, "copy_blocks check launch");
+    e = launch_kernel(copy_blocks_kernel, dim3(n, (unsigned)gy), dim3(kCopyThreads), 0, stream,
+                      static_cast<uint4*>(pool), pairs, NB, blk_vec, dev_err);
     count_launch();
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "copy_blocks launch");
 }
@@ -211,7 +249,7 @@ pa_status launch_write_contiguous(const void* k, const void* v, void* k_buf, voi
                                   cudaStream_t stream) {
     if (T == 0) return PA_OK;
     const int row_vec = H_kv * D * 2 / 16;
-    const int grid = T < 152 * 16 ? T : 152 * 16;
+    const int grid = token_grid(T);
     cudaError_t e = launch_kernel(write_contiguous_kernel, dim3(grid), dim3(128), 0, stream,
                                   static_cast<const uint4*>(k), static_cast<const uint4*>(v),
                                   static_cast<uint4*>(k_buf), static_cast<uint4*>(v_buf), req_ids, positions, T, N_max,
