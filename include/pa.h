@@ -224,8 +224,10 @@ pa_status pa_prefill(void* out, pa_dtype out_dtype, const void* q, const void* p
  *   the process exits.  A batch whose pa_decode_workspace_bytes(...) exceeds
  *   it is rejected with PA_ERR_UNSUPPORTED and a message; nothing is launched.
  * - The first call on a device looks up the array's device address for that
- *   device (cudaGetSymbolAddress with the device current); make that first
- *   call before any stream capture.  The call allocates nothing.
+ *   device (cudaGetSymbolAddress with the device current) and caches it with
+ *   the context's unique ID; the first call after the context is torn down
+ *   (cudaDeviceReset) looks it up again.  Make that first call before any
+ *   stream capture.  The call allocates nothing.
  * - All calls share the one array and it keeps the last call's contents; the
  *   kernels rewrite every part of it they read, so nothing needs clearing.
  *   Calls that overlap on the GPU (different streams, or threads) race on it:

@@ -8,6 +8,8 @@
 // For them the workspace lives in `g_decode_scratch`, a file-scope device
 // array that is part of the loaded module, so every GPU that loads libpa.so
 // holds it for the life of the process.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "pa_internal.h"
@@ -17,10 +19,52 @@ namespace pa {
 static __device__ __align__(256) unsigned char g_decode_scratch[PA_STATIC_WORKSPACE_BYTES];
 
 // In host code `g_decode_scratch` names a host-side stand-in, not device
-// memory; the device address comes from cudaGetSymbolAddress, once per device.
+// memory; the device address comes from cudaGetSymbolAddress, called with the
+// device current.  The address belongs to the module as loaded into one CUDA
+// context, so it is cached per device together with that context's unique ID
+// (cuCtxGetId): after cudaDeviceReset, or any other teardown of the context,
+// the next call finds a new ID and looks the address up again instead of
+// handing the kernels a stale one.
 constexpr int kMaxDevices = 64;
 static std::mutex g_scratch_mu;
-static void* g_scratch_ptr[kMaxDevices];
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    void* ptr;
+};
+static ScratchEntry g_scratch[kMaxDevices];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+static void* driver_fn(const char* name) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return f;
+}
+
+// Unique ID of the context current on this thread (0 when there is none yet).
+static pa_status current_ctx_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        get_current = reinterpret_cast<CtxGetCurrentFn>(driver_fn("cuCtxGetCurrent"));
+        get_id = reinterpret_cast<CtxGetIdFn>(driver_fn("cuCtxGetId"));
+    });
+    if (!get_current || !get_id) return fail(PA_ERR_CUDA, "cuCtxGetCurrent / cuCtxGetId are not available");
+    CUcontext ctx = nullptr;
+    CUresult r = get_current(&ctx);
+    if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuCtxGetCurrent failed (CUresult %d)", (int)r);
+    *id = 0;
+    if (ctx) {
+        r = get_id(ctx, id);
+        if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuCtxGetId failed (CUresult %d)", (int)r);
+    }
+    return PA_OK;
+}
 
 static pa_status scratch_address(void** out) {
     int dev = 0;
@@ -28,13 +72,22 @@ static pa_status scratch_address(void** out) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return fail(PA_ERR_UNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    unsigned long long id = 0;
+    pa_status st = current_ctx_id(&id);
+    if (st != PA_OK) return st;
+    ScratchEntry& ent = g_scratch[dev];
+    if (id == 0 || ent.ptr == nullptr || ent.ctx_id != id) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);  // makes the device's primary context current if needed
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static decode workspace)");
-        g_scratch_ptr[dev] = p;
+        if (id == 0) {
+            st = current_ctx_id(&id);
+            if (st != PA_OK) return st;
+        }
+        ent.ctx_id = id;
+        ent.ptr = p;
     }
-    *out = g_scratch_ptr[dev];
+    *out = ent.ptr;
     return PA_OK;
 }
 
