@@ -8,11 +8,17 @@ One step = one decode step of the whole hot path for 256 sequences:
   partition merge).
 Inputs: 256 sequences, lengths lognormal (median 1000, sigma 1.0, cap 8192),
 32 query / 8 KV heads, D 128, B 16, bf16 N(0,1), shuffled physical blocks
-(~1.65 GB of K/V per step: larger than L2, so no flush is needed).
+(1.50 GB of K/V per step at the seeded lengths: larger than L2, so no flush
+is needed).
 
 Output: one JSON line (rank 0).  `value` is KV-read GB/s over whole steps;
 `roofline` is the attention kernel alone against the measured HBM copy rate;
 `cpu_baseline` / `--impl reference` time the fp64 oracle on host cores.
+The same line carries, under `workloads`, the other decode workloads (OPT-13B,
+the copy-on-write parallel-sampling step, the 32K Yi-34B context paged at three
+block sizes and in the contiguous layout), the cache write and the block copy
+timed on their own, and the tensor-core prefill (about a second each;
+`--no-workloads` skips them).
 """
 from __future__ import annotations
 
@@ -52,6 +58,11 @@ def parse():
     ap.add_argument("--seqs", type=int, default=256,
                     help="sequences (256 is the benchmarked workload; fewer for small profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads, cache ops and prefill in the default run")
+    ap.add_argument("--clock-window", type=float, default=1.5,
+                    help="seconds of the same decode steps replayed right after the timed region under the clock "
+                         "sampler (not part of value)")
     ap.add_argument("--measure", choices=["decode", "swap", "prefill", "configs", "vmm"], default="decode",
                     help="swap: pa_swap_blocks device<->pinned host; prefill: chunked paged prefill (tcgen05)")
     return ap.parse_args()
@@ -97,7 +108,7 @@ def config_dict(w: W.Workload, pt: int) -> dict:
         "ctx": "lognormal(median 1000, sigma 1.0), capped at 8192",
         "ctx_tokens_first_step": int(w.ctx.sum()),
         "partition_tokens": 512 if pt == 0 else pt,
-        "l2": "inputs larger than L2 (about 1.65 GB of K/V per step), no flush",
+        "l2": "inputs larger than L2 (1.50 GB of K/V per step at the seeded lengths), no flush",
     }
 
 
@@ -245,12 +256,16 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        """Samples taken between mark('t0') and mark('t1') (the timed region)."""
+        """Samples taken from mark('t0') (start of the timed region) to mark('t2') (end of the clock window that
+        replays the same steps right after it; mark('t1') when there is none), and how many fell inside the timed
+        region itself."""
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         t0, t1 = getattr(self, "t0", 0.0), getattr(self, "t1", float("inf"))
+        t_end = getattr(self, "t2", t1)
+        in_timed = 0
         for t, ln in self.lines:
-            if not (t0 <= t <= t1 + 0.025):
+            if not (t0 <= t <= t_end + 0.025):
                 continue
             p = [x.strip() for x in ln.split(",")]
             if len(p) < 9:
@@ -260,13 +275,17 @@ class ClockSampler:
                 mx.append(float(p[2]))
             except ValueError:
                 continue
+            in_timed += t <= t1 + 0.025
             for name, val in zip(names, p[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "samples_in_timed_region": int(in_timed),
+                "window_s": round(t_end - t0, 3),
+                "note": "nvidia-smi every 20 ms over the timed region and the same decode steps replayed right "
+                        "after it (not part of value)"}
 
 
 DEVICE_HDR = os.path.join(ROOT, "paged_kv_cache_302_gb300", "csrc", "pa_device.cuh")
@@ -379,7 +398,16 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         clk.mark("t1")
-    launches = pa.launch_count() - launches0
+        launches = pa.launch_count() - launches0
+        # clock window: the timed region is a few milliseconds, shorter than the sampler's period, so the same
+        # steps (each rewrites its own token and reads its own lengths: replaying them changes nothing) run again
+        # for a second or so under the sampler
+        t_end = time.time() + args.clock_window
+        while time.time() < t_end:
+            for i in range(args.warmup, nsteps):
+                step(i)
+            torch.cuda.synchronize()
+        clk.mark("t2")
     t_dev = e0.elapsed_time(e1) * 1e-3
     # the attention kernel alone: the same steps again with events around it (an event between the
     # schedule and attention kernels stops their overlap, so these runs are not part of `value`)
@@ -418,6 +446,12 @@ def run_ours(args):
                "single_thread_value": rate1,
                "single_thread_sample": f"{seqs1} sequences, {secs1:.1f} s", "cpu_model": cpu_model()}
 
+    # ---- the other workloads, the cache ops alone and the prefill (rank 0, N = 1 only; about a second each)
+    extra = {}
+    if rank == 0 and world == 1 and not args.no_workloads:
+        extra = {"workloads": measure_workloads(hbm), "cache_ops": measure_cache_ops(hbm),
+                 "prefill": measure_prefill()}
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -434,6 +468,7 @@ def run_ours(args):
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
             "clocks": clk.summary(),
+            **extra,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -591,16 +626,15 @@ def run_swap(args):
     return 0
 
 
-def run_prefill(args):
+def measure_prefill(steps: int = 10, warmup: int = 3) -> list:
     """Chunked paged prefill on the tensor cores: Llama-3-8B shapes (32 q / 8 KV heads, D 128, B 16), 16 sequences
     whose last 2048 of 4096 tokens are the chunk (K/V already in the pool); bf16, then the same shapes in fp16
     (whose probabilities need one value product instead of two).  FLOPs count the causal score and value
-    products actually needed: 4 * D * (position + 1) per query row and head."""
+    products actually needed: 4 * D * (position + 1) per query row and head.  Calls back to back, CUDA events."""
     import torch
 
     import paged_kv_cache_302_gb300 as pa
 
-    torch.cuda.set_device(0)
     N, ctx_len, chunk, H_q, H_kv, D, B = 16, 4096, 2048, 32, 8, 128, 16
     nb = ctx_len // B
     NB = N * nb + 64
@@ -612,30 +646,41 @@ def run_prefill(args):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     pos = np.arange(ctx_len - chunk, ctx_len, dtype=np.float64)
     flops = N * H_q * 4.0 * D * float((pos + 1).sum())
-    peak = 1900.0
+    peak, peak_src = 1900.0, "fallback (1.9 PFLOP/s bf16, one earlier GB300 measurement)"
     try:
         peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"])
+        peak_src = "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"
     except Exception:
         pass
+    res = []
     for dt, name in ((torch.bfloat16, "bf16"), (torch.float16, "f16")):
         pool = torch.empty((NB, B, 2, H_kv, D), dtype=dt, device="cuda").normal_()
         q = torch.empty((N * chunk, H_q, D), dtype=dt, device="cuda").normal_()
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             pa.pa_prefill(out, q, pool, tables, ctx, q_start, chunk, dev_err=err)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for _ in range(args.steps):
+        for _ in range(steps):
             pa.pa_prefill(out, q, pool, tables, ctx, q_start, chunk, dev_err=err)
         e1.record()
         torch.cuda.synchronize()
         assert int(err.item()) == 0
-        t = e0.elapsed_time(e1) * 1e-3 / args.steps
+        t = e0.elapsed_time(e1) * 1e-3 / steps
         tf = flops / t / 1e12
         # the fp16 dense tensor rate equals the bf16 one on this GPU
-        print(json.dumps({"measure": "pa_prefill", "kv_dtype": name, "unit": "TFLOP/s", "value": tf,
-                          "ms_per_call": t * 1e3, "peak_bf16_tflops": peak, "frac": tf / peak, "seqs": N,
-                          "ctx": ctx_len, "chunk": chunk, "flops_per_call": flops, "steps": args.steps}), flush=True)
+        res.append({"kv_dtype": name, "unit": "TFLOP/s", "value": tf, "ms_per_call": t * 1e3,
+                    "peak_bf16_tflops": peak, "peak_source": peak_src, "frac": tf / peak, "seqs": N, "ctx": ctx_len,
+                    "chunk": chunk, "flops_per_call": flops, "calls": steps})
         del pool, q
+    return res
+
+
+def run_prefill(args):
+    import torch
+
+    torch.cuda.set_device(0)
+    for r in measure_prefill(args.steps, args.warmup):
+        print(json.dumps({"measure": "pa_prefill", **r}), flush=True)
     return 0
 
 
@@ -663,52 +708,84 @@ def _time_decode(fn, att_ev, reps=20, warm=3):
     return t_call, float(np.median(ta))
 
 
-def run_configs(args):
-    """Decode throughput on the other workloads: OPT-13B MHA, the copy-on-write parallel-sampling batch
-    (logical and unique K/V bytes) and the Yi-34B-shaped 32K context, paged at B = 8 / 16 / 32 and in the
-    contiguous per-request layout (the unpaged comparison).  One JSON line per workload."""
+def _time_cold(fn, reps=15, warm=3):
+    """Median seconds of one call with L2 flushed before it (a 512 MB buffer is written between calls), CUDA
+    events around the call alone."""
+    import torch
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(warm):
+        fn()
+    ts = []
+    for _ in range(reps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e-3)
+    del flush
+    return float(np.median(ts))
+
+
+def _paged_case(w, alloc_fn=None):
+    """Allocator state, device tables and an N(0,1) pool / queries (drawn on the device) for a workload."""
     import torch
 
     import paged_kv_cache_302_gb300 as pa
 
-    torch.cuda.set_device(0)
-    hbm, _ = peaks()
+    a = pa.BlockAllocator(w.NB, w.B, w.free_order)
+    extra = None
+    if alloc_fn is None:
+        for s in range(w.N):
+            a.add_seq(s)
+            a.append_slots(s, int(w.ctx[s]))
+    else:
+        extra = alloc_fn(a)
+    tables, ctx = a.block_tables(list(range(w.N)), w.max_blocks_per_seq())
+    dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
+    pool = torch.empty((w.NB, w.B, 2, w.H_kv, w.D), dtype=dt, device="cuda").normal_()
+    q = torch.empty((w.N, w.H_q, w.D), dtype=dt, device="cuda").normal_()
+    out = torch.empty((w.N, w.H_q, w.D), device="cuda")
+    tab, cx = torch.from_numpy(tables).cuda(), torch.from_numpy(ctx).cuda()
+    ws = torch.empty(pa.pa_decode_workspace_bytes(w.N, w.H_q, w.H_kv, w.D, int(ctx.max()), 0), dtype=torch.uint8,
+                     device="cuda")
+    return dict(a=a, tables=tables, ctx=ctx, pool=pool, q=q, out=out, tab=tab, cx=cx, ws=ws, extra=extra)
+
+
+def measure_workloads(hbm: float) -> dict:
+    """Decode throughput on the other workloads (whole pa_decode call back to back, and the attention kernel
+    alone): OPT-13B MHA; the copy-on-write parallel-sampling batch, decode on logical and unique K/V bytes and a
+    whole device step (the 224 copy-on-write block copies, the cache write of every sample's new tokens, the
+    decode); the Yi-34B-shaped 32K context paged at B = 8 / 16 / 32 and in the contiguous per-request layout (the
+    unpaged comparison).  Pools and queries are N(0,1) drawn on the device (throughput does not depend on the
+    values; parity at these sizes is the test suite's)."""
+    import torch
+
+    import paged_kv_cache_302_gb300 as pa
+
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     ev = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+    res = {}
 
-    def paged_case(w, alloc_fn=None):
-        a = pa.BlockAllocator(w.NB, w.B, w.free_order)
-        if alloc_fn is None:
-            for s in range(w.N):
-                a.add_seq(s)
-                a.append_slots(s, int(w.ctx[s]))
-        else:
-            alloc_fn(a)
-        tables, ctx = a.block_tables(list(range(w.N)), w.max_blocks_per_seq())
-        dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
-        pool = torch.empty((w.NB, w.B, 2, w.H_kv, w.D), dtype=dt, device="cuda").normal_()
-        q = torch.empty((w.N, w.H_q, w.D), dtype=dt, device="cuda").normal_()
-        out = torch.empty((w.N, w.H_q, w.D), device="cuda")
-        tab, cx = torch.from_numpy(tables).cuda(), torch.from_numpy(ctx).cuda()
-        ws = torch.empty(pa.pa_decode_workspace_bytes(w.N, w.H_q, w.H_kv, w.D, int(ctx.max()), 0), dtype=torch.uint8,
-                         device="cuda")
-        return a, tables, ctx, pool, q, out, tab, cx, ws
+    def decode_fn(c):
+        return lambda e: pa.pa_decode(c["out"], c["q"], c["pool"], c["tab"], c["cx"], int(c["ctx"].max()),
+                                      workspace=c["ws"], dev_err=err, attend_events=e)
 
-    def line(name, nbytes, t_step, t_att, **extra):
-        print(json.dumps({"measure": "decode_workload", "workload": name, "unit": "GB/s",
-                          "kv_bytes": nbytes, "step_gbs": nbytes / t_step / 1e9, "attend_gbs": nbytes / t_att / 1e9,
-                          "attend_frac_of_hbm": nbytes / t_att / 1e9 / hbm, "us_per_call": t_step * 1e6, **extra}),
-              flush=True)
+    def rates(nbytes, t, ta):
+        return {"kv_bytes": nbytes, "step_gbs": nbytes / t / 1e9, "attend_gbs": nbytes / ta / 1e9,
+                "attend_frac_of_hbm": nbytes / ta / 1e9 / hbm, "us_per_call": t * 1e6}
 
     # OPT-13B-shaped MHA
     w = W.opt13b()
-    a, tables, ctx, pool, q, out, tab, cx, ws = paged_case(w)
-    nbytes = int(ctx.astype(np.int64).sum()) * 2 * w.H_kv * w.D * 2
-    t, ta = _time_decode(lambda e: pa.pa_decode(out, q, pool, tab, cx, int(ctx.max()), workspace=ws, dev_err=err,
-                                                attend_events=e), ev)
-    line("opt13b_mha_fp16", nbytes, t, ta)
+    c = _paged_case(w)
+    nbytes = int(c["ctx"].astype(np.int64).sum()) * 2 * w.H_kv * w.D * 2
+    res["opt13b_mha_fp16"] = rates(nbytes, *_time_decode(decode_fn(c), ev))
+    del c
 
-    # parallel sampling with copy-on-write prefix sharing
+    # parallel sampling with copy-on-write prefix sharing: prompts written, forked to 8 samples, then one batched
+    # append of every sample's divergent tokens (host), the copy-on-write copies, the cache write and the decode
     w = W.cow()
 
     def cow_alloc(a):
@@ -718,45 +795,131 @@ def run_configs(args):
             a.append_slots(base, w.prompt_len)
             for j in range(1, w.samples):
                 a.fork(base, base + j)
-        a.append_batch(list(range(w.N)), w.extra)
+        t0 = time.perf_counter()
+        slots, pairs = a.append_batch(list(range(w.N)), w.extra)
+        return slots, pairs, time.perf_counter() - t0
 
-    a, tables, ctx, pool, q, out, tab, cx, ws = paged_case(w, cow_alloc)
+    c = _paged_case(w, cow_alloc)
+    slots, pairs, t_host = c["extra"]
     per_tok = 2 * w.H_kv * w.D * 2
-    logical = int(ctx.astype(np.int64).sum()) * per_tok
-    uniq = len(set(tables[tables >= 0].tolist())) * w.B * per_tok
-    t, ta = _time_decode(lambda e: pa.pa_decode(out, q, pool, tab, cx, int(ctx.max()), workspace=ws, dev_err=err,
-                                                attend_events=e), ev)
-    line("cow_parallel_sampling", logical, t, ta, unique_kv_bytes=uniq, attend_unique_gbs=uniq / ta / 1e9,
-         attend_unique_frac_of_hbm=uniq / ta / 1e9 / hbm)
+    logical = int(c["ctx"].astype(np.int64).sum()) * per_tok
+    uniq = len(set(c["tables"][c["tables"] >= 0].tolist())) * w.B * per_tok
+    t, ta = _time_decode(decode_fn(c), ev)
+    r = rates(logical, t, ta)
+    r.update(unique_kv_bytes=uniq, attend_unique_gbs=uniq / ta / 1e9, attend_unique_frac_of_hbm=uniq / ta / 1e9 / hbm)
+    d_pairs = torch.from_numpy(np.ascontiguousarray(pairs)).cuda()
+    d_slots = torch.from_numpy(slots).cuda()
+    T = int(slots.size)
+    k = torch.empty((T, w.H_kv, w.D), dtype=torch.bfloat16, device="cuda").normal_()
+    v = torch.empty_like(k)
+
+    def cow_step():
+        pa.pa_copy_blocks(c["pool"], d_pairs, dev_err=err)
+        pa.pa_reshape_and_cache(k, v, c["pool"], d_slots, dev_err=err)
+        decode_fn(c)(None)
+
+    for _ in range(3):
+        cow_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 20
+    e0.record()
+    for _ in range(reps):
+        cow_step()
+    e1.record()
+    torch.cuda.synchronize()
+    t_step = e0.elapsed_time(e1) * 1e-3 / reps
+    blk = w.B * per_tok
+    t_copy = _time_cold(lambda: pa.pa_copy_blocks(c["pool"], d_pairs, dev_err=err))
+    r["cow_step"] = {
+        "what": "device part of one step: pa_copy_blocks of the copy-on-write pairs, pa_reshape_and_cache of every "
+                "sample's new tokens, pa_decode over all sequences; 20 steps back to back",
+        "cow_pairs": int(pairs.shape[0]), "new_tokens": T, "us_per_step": t_step * 1e6,
+        "logical_kv_gbs": logical / t_step / 1e9,
+        "host_append_batch_us": t_host * 1e6,
+        "copy_blocks_us": t_copy * 1e6,
+        "copy_blocks_gbs": 2 * pairs.shape[0] * blk / t_copy / 1e9,
+    }
+    res["cow_parallel_sampling"] = r
+    del c, k, v
 
     # Yi-34B-shaped long context, paged at three block sizes and contiguous
     for B in (8, 16, 32):
         w = W.yi34b_long(B=B)
-        a, tables, ctx, pool, q, out, tab, cx, ws = paged_case(w)
-        nbytes = int(ctx.astype(np.int64).sum()) * 2 * w.H_kv * w.D * 2
-        t, ta = _time_decode(lambda e: pa.pa_decode(out, q, pool, tab, cx, int(ctx.max()), workspace=ws,
-                                                    dev_err=err, attend_events=e), ev)
-        res = dict(paged_step_gbs=nbytes / t / 1e9, paged_attend_gbs=nbytes / ta / 1e9)
-        # the same K/V in per-request buffers at request offsets req * S
-        N_max, S_max = w.N, int(ctx.max())
+        c = _paged_case(w)
+        nbytes = int(c["ctx"].astype(np.int64).sum()) * 2 * w.H_kv * w.D * 2
+        t, ta = _time_decode(decode_fn(c), ev)
+        N_max, S_max = w.N, int(c["ctx"].max())
         req = torch.from_numpy(W.request_ids(w, N_max)).cuda()
         t_idx = torch.arange(S_max, device="cuda")
         kb = torch.empty((N_max, S_max, w.H_kv, w.D), dtype=torch.bfloat16, device="cuda")
         vb = torch.empty_like(kb)
         for si in range(w.N):
-            phys = tab[si, t_idx // B].long()
-            kb[req[si]] = pool[phys, t_idx % B, 0]
-            vb[req[si]] = pool[phys, t_idx % B, 1]
-        out2 = torch.empty_like(out)
-        tc, tca = _time_decode(lambda e: pa.pa_decode_contiguous(out2, q, kb, vb, req, cx, int(ctx.max()),
-                                                                 workspace=ws, dev_err=err, attend_events=e), ev)
+            phys = c["tab"][si, t_idx // B].long()
+            kb[req[si]] = c["pool"][phys, t_idx % B, 0]
+            vb[req[si]] = c["pool"][phys, t_idx % B, 1]
+        out2 = torch.empty_like(c["out"])
+        tc, tca = _time_decode(lambda e: pa.pa_decode_contiguous(out2, c["q"], kb, vb, req, c["cx"], S_max,
+                                                                 workspace=c["ws"], dev_err=err, attend_events=e), ev)
         torch.cuda.synchronize()
-        assert torch.equal(out, out2), "paged and contiguous outputs differ"
-        line(f"yi34b_long_B{B}", nbytes, t, ta, contiguous_step_gbs=nbytes / tc / 1e9,
-             contiguous_attend_gbs=nbytes / tca / 1e9, paged_over_contiguous_step=tc / t,
-             paged_over_contiguous_attend=tca / ta)
-        del kb, vb, pool
-    assert int(err.item()) == 0
+        assert torch.equal(c["out"], out2), "paged and contiguous outputs differ"
+        r = rates(nbytes, t, ta)
+        r.update(contiguous_step_gbs=nbytes / tc / 1e9, contiguous_attend_gbs=nbytes / tca / 1e9,
+                 paged_over_contiguous_step=tc / t, paged_over_contiguous_attend=tca / ta)
+        res[f"yi34b_long_B{B}"] = r
+        del kb, vb, c
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error flags {int(err.item())}"
+    return res
+
+
+def measure_cache_ops(hbm: float) -> dict:
+    """pa_reshape_and_cache and pa_copy_blocks timed on their own (L2 flushed before each call, CUDA events around
+    the call, median), at Llama-3-8B shapes (one token = 8 KV heads x 128 x bf16 for K and for V: 4 KB; one block
+    = 16 tokens: 64 KB): the cache write of one decode step (256 tokens) and of a 64K-token prefill, the block
+    copy of 224 pairs (the copy-on-write step of the parallel-sampling workload) and of 8192 pairs.  GB/s count
+    the bytes read plus the bytes written."""
+    import torch
+
+    import paged_kv_cache_302_gb300 as pa
+
+    H_kv, D, B = 8, 128, 16
+    per_tok = 2 * H_kv * D * 2
+    NB = 20000
+    rng = np.random.default_rng(17)
+    pool = torch.empty((NB, B, 2, H_kv, D), dtype=torch.bfloat16, device="cuda").normal_()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    res = {}
+    for T in (256, 65536):
+        slots = torch.from_numpy(rng.permutation(NB * B)[:T].astype(np.int64)).cuda()
+        k = torch.empty((T, H_kv, D), dtype=torch.bfloat16, device="cuda").normal_()
+        v = torch.empty_like(k)
+        t = _time_cold(lambda: pa.pa_reshape_and_cache(k, v, pool, slots, dev_err=err))
+        res[f"reshape_and_cache_{T}_tokens"] = {"us": t * 1e6, "gbs": 2 * T * per_tok / t / 1e9,
+                                                "frac_of_hbm": 2 * T * per_tok / t / 1e9 / hbm}
+    for n in (224, 8192):
+        ids = rng.permutation(NB)[: 2 * n].astype(np.int64)
+        pairs = torch.from_numpy(np.stack([ids[:n], ids[n:]], axis=1)).cuda()
+        t = _time_cold(lambda: pa.pa_copy_blocks(pool, pairs, dev_err=err))
+        res[f"copy_blocks_{n}_pairs"] = {"us": t * 1e6, "gbs": 2 * n * B * per_tok / t / 1e9,
+                                         "frac_of_hbm": 2 * n * B * per_tok / t / 1e9 / hbm}
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error flags {int(err.item())}"
+    return res
+
+
+def run_configs(args):
+    """The other workloads, the cache ops and the prefill, one JSON line each (the default run embeds the same
+    figures in its line)."""
+    import torch
+
+    torch.cuda.set_device(0)
+    hbm, _ = peaks()
+    for name, r in measure_workloads(hbm).items():
+        print(json.dumps({"measure": "decode_workload", "workload": name, "unit": "GB/s", **r}), flush=True)
+    print(json.dumps({"measure": "cache_ops", **measure_cache_ops(hbm)}), flush=True)
+    for r in measure_prefill():
+        print(json.dumps({"measure": "pa_prefill", **r}), flush=True)
     return 0
 
 

@@ -47,7 +47,14 @@ def test_clock_summary_keeps_only_the_timed_window_and_reports_throttle_reasons(
     s = c.summary()
     assert s["samples"] == 3 and s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
     assert s["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert s["samples_in_timed_region"] == 3
     assert b.ClockSampler(0).summary()["reasons"] == ["unsampled"]
+    # with a clock window after the timed region (mark t2) its samples count too, and the ones inside the
+    # timed region are told apart
+    c.t2 = 25.0
+    c.lines.insert(4, (22.0, row.format(sm=2055, hw="Not Active", pc="Not Active")))
+    s = c.summary()
+    assert s["samples"] == 4 and s["samples_in_timed_region"] == 3 and s["window_s"] == 15.0
 
 
 def test_attention_source_hash_spans_the_attention_kernel():
