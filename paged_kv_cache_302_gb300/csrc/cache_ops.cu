@@ -60,21 +60,21 @@ pa_status launch_reshape_and_cache(const void* k, const void* v, void* pool, con
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "reshape_and_cache launch");
 }
 
+// grid.x = pair index (plus the check CTAs below), grid.y = chunk of the block; each thread moves kUnroll vectors
+// per chunk with all loads issued before the stores.
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+
 // Chained pairs (a destination that is also a source, or a destination named twice) make the result of a copy
-// call depend on the order of the copies; they are flagged, in one pass over the pairs.  CTA r owns the block ids
-// [r * kCheckIds, (r + 1) * kCheckIds): it marks the destinations that fall in its range in a shared-memory bitmap
-// (a bit found already set is a repeated destination), then looks up the sources in its range.  One CTA covers
-// 262144 block ids, so a pool of up to that many blocks is checked by a single CTA reading every pair twice.
-constexpr int kCheckThreads = 1024;
-constexpr int kCheckWords = 8192;  // 32 KB of bitmap
+// call depend on the order of the copies; they are flagged, in one pass over the pairs, by kCheckIds-wide ranges
+// of block ids: check CTA r (grid.x = n + r, grid.y = 0) marks the destinations that fall in its range in a
+// shared-memory bitmap (a bit found already set is a repeated destination), then looks up the sources in its
+// range.  One check CTA covers 131072 block ids; the check runs beside the copies, in the same launch.
+constexpr int kCheckWords = 4096;  // 16 KB of bitmap
 constexpr int64_t kCheckIds = (int64_t)kCheckWords * 32;
 
-__global__ void __launch_bounds__(kCheckThreads) check_pairs_kernel(const int64_t* __restrict__ pairs, int n,
-                                                                    int* err) {
-    griddep_wait();
-    griddep_launch_dependents();
-    __shared__ uint32_t bits[kCheckWords];
-    const int64_t lo = (int64_t)blockIdx.x * kCheckIds;
+__device__ __forceinline__ void check_pairs(const int64_t* __restrict__ pairs, int n, int64_t lo, uint32_t* bits,
+                                            int* err) {
     for (int i = threadIdx.x; i < kCheckWords; i += blockDim.x) bits[i] = 0;
     __syncthreads();
     bool bad = false;
@@ -93,17 +93,17 @@ __global__ void __launch_bounds__(kCheckThreads) check_pairs_kernel(const int64_
     if (__syncthreads_or(bad) && threadIdx.x == 0) flag_error(err, PA_DEV_ERR_BLOCK);
 }
 
-// grid.x = pair index, grid.y = chunk of the block; each thread moves
-// kUnroll vectors per chunk with all loads issued before the stores.
-constexpr int kCopyThreads = 256;
-constexpr int kCopyUnroll = 4;
-
 __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(uint4* __restrict__ pool,
-                                                                   const int64_t* __restrict__ pairs, int NB,
+                                                                   const int64_t* __restrict__ pairs, int n, int NB,
                                                                    int64_t blk_vec, int* err) {
     griddep_wait();
     griddep_launch_dependents();
+    __shared__ uint32_t bits[kCheckWords];
     const int i = blockIdx.x;
+    if (i >= n) {
+        if (blockIdx.y == 0) check_pairs(pairs, n, (int64_t)(i - n) * kCheckIds, bits, err);
+        return;
+    }
     const int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
     if (src < 0 || src >= NB || dst < 0 || dst >= NB) {
         if (threadIdx.x == 0 && blockIdx.y == 0) flag_error(err, PA_DEV_ERR_BLOCK);
@@ -134,12 +134,10 @@ pa_status launch_copy_blocks(void* pool, const int64_t* pairs, int n, int NB, in
     const int64_t chunk = (int64_t)kCopyThreads * kCopyUnroll;
     int64_t gy = (blk_vec + chunk - 1) / chunk;
     if (gy > 65535) gy = 65535;
-    cudaError_t e = launch_kernel(check_pairs_kernel, dim3((unsigned)(((int64_t)NB + kCheckIds - 1) / kCheckIds)),
-                                  dim3(kCheckThreads), 0, stream, pairs, n, dev_err);
-    count_launch();
-    if (e != cudaSuccess) return cuda_fail(e, "copy_blocks check launch");
-    e = launch_kernel(copy_blocks_kernel, dim3(n, (unsigned)gy), dim3(kCopyThreads), 0, stream,
-                      static_cast<uint4*>(pool), pairs, NB, blk_vec, dev_err);
+    const int64_t gx = (int64_t)n + ((int64_t)NB + kCheckIds - 1) / kCheckIds;
+    if (gx > 0x7fffffff) return fail(PA_ERR_INVALID, "too many copy pairs: %d", n);
+    cudaError_t e = launch_kernel(copy_blocks_kernel, dim3((unsigned)gx, (unsigned)gy), dim3(kCopyThreads), 0, stream,
+                                  static_cast<uint4*>(pool), pairs, n, NB, blk_vec, dev_err);
     count_launch();
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "copy_blocks launch");
 }

@@ -785,10 +785,14 @@ __global__ void __launch_bounds__(kAttnThreads) attend_kernel(const __grid_const
 // ============================================================================= 3. partition merge
 
 // One warp per output row, 8 rows per CTA, so the whole merge is one wave of
-// short-lived warps.  Lane j holds the weight 2^(m2_p - M) of partitions
-// p = j, j+32, ...; the weighted sum over partitions broadcasts each weight
-// and keeps eight partitions' loads in flight.
+// short-lived warps.  The merge is latency bound (its inputs sit in L2), so a
+// warp issues every load of up to kMergeChunk partitions -- lane j's m2 and l
+// of partition j, and each lane's D/32 columns of every partition's acc --
+// before it uses any of them: one L2 round trip after the partition count
+// instead of one per dependent step.  Longer rows take further chunks, the
+// running maximum and sums rescaled between chunks.
 constexpr int kReduceWarps = 8;
+constexpr int kMergeChunk = 8;
 
 template <typename OutT, int D>
 __global__ void __launch_bounds__(kReduceWarps * 32) partition_reduce_kernel(
@@ -809,33 +813,51 @@ __global__ void __launch_bounds__(kReduceWarps * 32) partition_reduce_kernel(
     const float* mr = m2 + (size_t)r * P;
     const float* lr = l + (size_t)r * P;
     const float* ar = acc + (size_t)r * P * D + lane * V;
-    float M = -INFINITY;
-    for (int i = lane; i < np; i += 32) M = fmaxf(M, mr[i]);
-#pragma unroll
-    for (int k = 16; k > 0; k >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, k));
-    float o[V], den = 0.f;
+    float M = -INFINITY, den = 0.f, o[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) o[v] = 0.f;
-    for (int base = 0; base < np; base += 32) {
-        const int mine = base + lane;
-        const float w = mine < np ? fast_exp2(mr[mine] - M) : 0.f;
-        if (mine < np) den += w * lr[mine];
-        const int n = min(32, np - base);
-#pragma unroll 8
-        for (int j = 0; j < n; ++j) {
-            const float wj = __shfl_sync(0xffffffffu, w, j);
-            const float* a = ar + (size_t)(base + j) * D;
-            if constexpr (V == 4) {
-                const float4 x = *reinterpret_cast<const float4*>(a);
-                o[0] += wj * x.x;
-                o[1] += wj * x.y;
-                o[2] += wj * x.z;
-                o[3] += wj * x.w;
+    for (int base = 0; base < np; base += kMergeChunk) {
+        const int n = min(kMergeChunk, np - base);
+        // every load of the chunk first
+        const float mv = lane < n ? mr[base + lane] : -INFINITY;
+        const float lv = lane < n ? lr[base + lane] : 0.f;
+        float a[kMergeChunk][V];
+#pragma unroll
+        for (int j = 0; j < kMergeChunk; ++j) {
+            if (j < n) {
+                const float* src = ar + (size_t)(base + j) * D;
+                if constexpr (V == 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(src);
+                    a[j][0] = x.x;
+                    a[j][1] = x.y;
+                    a[j][2] = x.z;
+                    a[j][3] = x.w;
+                } else {
+                    const float2 x = *reinterpret_cast<const float2*>(src);
+                    a[j][0] = x.x;
+                    a[j][1] = x.y;
+                }
             } else {
-                const float2 x = *reinterpret_cast<const float2*>(a);
-                o[0] += wj * x.x;
-                o[1] += wj * x.y;
+#pragma unroll
+                for (int v = 0; v < V; ++v) a[j][v] = 0.f;
             }
+        }
+        float mc = mv;
+#pragma unroll
+        for (int k = 16; k > 0; k >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, k));
+        const float Mn = fmaxf(M, mc);  // finite: every partition holds at least one token
+        const float f = fast_exp2(M - Mn);  // 0 on the first chunk (M = -inf)
+        den *= f;
+#pragma unroll
+        for (int v = 0; v < V; ++v) o[v] *= f;
+        M = Mn;
+        const float w = lane < n ? fast_exp2(mv - Mn) : 0.f;
+        den += w * lv;
+#pragma unroll
+        for (int j = 0; j < kMergeChunk; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, w, j);
+#pragma unroll
+            for (int v = 0; v < V; ++v) o[v] += wj * a[j][v];
         }
     }
 #pragma unroll

@@ -70,9 +70,9 @@ def test_copy_blocks_bit_exact_and_flags():
 
 
 def test_copy_blocks_many_pairs_over_a_large_pool():
-    """20000 pairs over a pool of 300000 one-kilobyte blocks (the chained-pair check then spans two CTAs of block
-    ids): bit-exact against the oracle with no flag; chains and repeated destinations above the first 262144 ids
-    are flagged."""
+    """20000 pairs over a pool of 300000 one-kilobyte blocks (the chained-pair check then spans three ranges of
+    131072 block ids): bit-exact against the oracle with no flag; chains and repeated destinations in the upper
+    ranges are flagged."""
     rng = np.random.default_rng(21)
     NB, B, H, D = 300000, 4, 1, 64
     bits = W.normal_bits(rng, (NB, B, 2, H, D), "f16")
