@@ -381,16 +381,16 @@ def run_ours(args):
         pa.pa_decode(out, q_d[i], pool, tab, ctx_steps[i], max_ctx, partition_tokens=pt, workspace=ws,
                      dev_err=err, attend_events=events)
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches0 = pa.launch_count()
     with ClockSampler(local) as clk:
-        time.sleep(0.5)                      # let the sampler start
+        time.sleep(0.5)                      # let the sampler start (before the warm-up: no idle gap before timing)
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        launches0 = pa.launch_count()
         clk.mark("t0")
         e0.record(stream)
         for i in range(args.warmup, nsteps):
