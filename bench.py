@@ -652,23 +652,31 @@ def measure_prefill(steps: int = 10, warmup: int = 3) -> list:
         peak_src = "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"
     except Exception:
         pass
+    ws = torch.empty(pa.pa_prefill_workspace_bytes(N, H_kv, D, B, nb), dtype=torch.uint8, device="cuda")
     res = []
-    for dt, name in ((torch.bfloat16, "bf16"), (torch.float16, "f16")):
+    for dt, name, stage_v in ((torch.bfloat16, "bf16", True), (torch.bfloat16, "bf16", False),
+                              (torch.float16, "f16", False)):
         pool = torch.empty((NB, B, 2, H_kv, D), dtype=dt, device="cuda").normal_()
         q = torch.empty((N * chunk, H_q, D), dtype=dt, device="cuda").normal_()
+
+        def call():
+            pa.pa_prefill(out, q, pool, tables, ctx, q_start, chunk, workspace=ws, stage_v=stage_v, dev_err=err)
+
         for _ in range(warmup):
-            pa.pa_prefill(out, q, pool, tables, ctx, q_start, chunk, dev_err=err)
+            call()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(steps):
-            pa.pa_prefill(out, q, pool, tables, ctx, q_start, chunk, dev_err=err)
+            call()
         e1.record()
         torch.cuda.synchronize()
         assert int(err.item()) == 0
         t = e0.elapsed_time(e1) * 1e-3 / steps
         tf = flops / t / 1e12
         # the fp16 dense tensor rate equals the bf16 one on this GPU
-        res.append({"kv_dtype": name, "unit": "TFLOP/s", "value": tf, "ms_per_call": t * 1e3,
+        how = ("V staged as fp16 by a first kernel (included), one value product" if stage_v and name == "bf16"
+               else "P split into two bf16 parts, two value products" if name == "bf16" else "fp16 P, one product")
+        res.append({"kv_dtype": name, "value_product": how, "unit": "TFLOP/s", "value": tf, "ms_per_call": t * 1e3,
                     "peak_bf16_tflops": peak, "peak_source": peak_src, "frac": tf / peak, "seqs": N, "ctx": ctx_len,
                     "chunk": chunk, "flops_per_call": flops, "calls": steps})
         del pool, q

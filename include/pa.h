@@ -204,13 +204,26 @@ pa_status pa_decode_contiguous(void* out, pa_dtype out_dtype, const void* q, con
  * q_start[0] = 0 and q_start[N] = T; max_q_len >= every chunk length.
  * Runs on the tensor cores (tcgen05, accumulators in TMEM).  A chunk longer
  * than its context is flagged PA_DEV_ERR_CTX and not computed.
+ * workspace (nullable), ws_bytes >= pa_prefill_workspace_bytes(N, H_kv, D, B,
+ * MB) of device memory: with a bf16 cache a first kernel stages each
+ * sequence's V there as fp16, so the value product takes P in fp16, one
+ * product per key instead of two (the staging kernel's time is part of the
+ * call).  The conversion is exact: a (sequence, KV head) holding a V
+ * magnitude >= 65536, or a group of 32 keys with only magnitudes < 2^-10,
+ * is computed as without a workspace instead.  Without a
+ * workspace a bf16 cache takes P as a high and a low bf16 part (two products,
+ * the same precision).  fp16 caches ignore the workspace.  The workspace's
+ * contents need not be initialised; calls that overlap on the GPU must not
+ * share one.
  * Supported: kv_dtype F16/BF16, D in {64, 128}, B in {8, 16, 32},
- * H_q / H_kv <= 128, N <= 65535, scale > 0.  out, q and pool must be
- * 16-byte aligned, an fp32 out 32-byte aligned (PA_ERR_INVALID otherwise).
+ * H_q / H_kv <= 128, N <= 65535, scale > 0.  out, q, pool and workspace must
+ * be 16-byte aligned, an fp32 out 32-byte aligned (PA_ERR_INVALID otherwise).
  * ---------------------------------------------------------------------- */
+size_t pa_prefill_workspace_bytes(int N, int H_kv, int D, int B, int MB);
 pa_status pa_prefill(void* out, pa_dtype out_dtype, const void* q, const void* pool, const int32_t* block_tables,
                      const int32_t* ctx_lens, const int32_t* q_start, int N, int T, int H_q, int H_kv, int D, int B,
-                     int MB, int NB, int max_q_len, float scale, pa_dtype kv_dtype, int* dev_err, void* stream);
+                     int MB, int NB, int max_q_len, float scale, pa_dtype kv_dtype, void* workspace, size_t ws_bytes,
+                     int* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
  * pa_decode without a caller-provided workspace.  The pages have no

@@ -93,7 +93,9 @@ def _declare(L):
         "pa_vkv_free_reqid": ([P, i32], i32),
         "pa_vkv_reclaim": ([P], i32),
         "pa_vkv_mapped_pages": ([P, i32, P], i32),
-        "pa_prefill": ([P, i32, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, P, P], i32),
+        "pa_prefill": ([P, i32, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, P, sz, P, P],
+                       i32),
+        "pa_prefill_workspace_bytes": ([i32, i32, i32, i32, i32], sz),
         "pa_alloc_fork": ([P, i32, i32], i32),
         "pa_alloc_free_seq": ([P, i32], i32),
         "pa_alloc_block_table": ([P, i32, P, i32, P], i32),
@@ -339,9 +341,18 @@ def pa_decode_contiguous(out, q, k_buf, v_buf, req_ids, ctx_lens, max_ctx, scale
     return out
 
 
-def pa_prefill(out, q, pool, block_tables, ctx_lens, q_start, max_q_len, scale=None, dev_err=None, stream=None):
+def pa_prefill_workspace_bytes(N, H_kv, D, B, MB) -> int:
+    n = load().pa_prefill_workspace_bytes(N, H_kv, D, B, MB)
+    if n == 0:
+        raise PAError(PA_ERR_INVALID, "invalid prefill workspace arguments")
+    return int(n)
+
+
+def pa_prefill(out, q, pool, block_tables, ctx_lens, q_start, max_q_len, scale=None, workspace=None,
+               stage_v=True, dev_err=None, stream=None):
     """Causal paged prefill: q, out [T, H_q, D]; q_start [N+1] int32 (device); chunks are the sequences' last
-    tokens, already written to the pool."""
+    tokens, already written to the pool.  A bf16 cache stages V as fp16 in `workspace` (allocated here when None
+    and stage_v is true); stage_v=False passes no workspace (P split into two bf16 parts instead)."""
     T, H_q, D = q.shape
     NB, B, _, H_kv, D2 = pool.shape
     N = ctx_lens.numel()
@@ -349,11 +360,16 @@ def pa_prefill(out, q, pool, block_tables, ctx_lens, q_start, max_q_len, scale=N
     if D2 != D or tuple(out.shape) != (T, H_q, D) or q.dtype != pool.dtype or q_start.numel() != N + 1:
         raise PAError(PA_ERR_INVALID, "shape/dtype mismatch")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    ws, ws_bytes = None, 0
+    if stage_v and pool.dtype == torch.bfloat16:
+        ws = _workspace(workspace, pa_prefill_workspace_bytes(N, H_kv, D, B, MB), q.device)
+        ws_bytes = ws.numel() * ws.element_size()
     L = load()
     _check(L.pa_prefill(_dev(out, "out"), _dtype_code(out.dtype), _dev(q, "q"), _dev(pool, "pool"),
                         _dev(block_tables, "block_tables", torch.int32), _dev(ctx_lens, "ctx_lens", torch.int32),
                         _dev(q_start, "q_start", torch.int32), N, T, H_q, H_kv, D, B, MB, NB, int(max_q_len), scale,
-                        _dtype_code(pool.dtype), _err_ptr(dev_err), _stream_ptr(stream)))
+                        _dtype_code(pool.dtype), _dev(ws, "workspace") if ws is not None else None, ws_bytes,
+                        _err_ptr(dev_err), _stream_ptr(stream)))
     return out
 
 

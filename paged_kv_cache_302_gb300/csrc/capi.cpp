@@ -282,9 +282,15 @@ pa_status pa_decode_contiguous(void* out, pa_dtype out_dtype, const void* q, con
     return launch_decode(a);
 }
 
+size_t pa_prefill_workspace_bytes(int N, int H_kv, int D, int B, int MB) {
+    PrefillWorkspace L;
+    return prefill_workspace_layout(N, H_kv, D, B, MB, &L) ? L.total : 0;
+}
+
 pa_status pa_prefill(void* out, pa_dtype out_dtype, const void* q, const void* pool, const int32_t* block_tables,
                      const int32_t* ctx_lens, const int32_t* q_start, int N, int T, int H_q, int H_kv, int D, int B,
-                     int MB, int NB, int max_q_len, float scale, pa_dtype kv_dtype, int* dev_err, void* stream) {
+                     int MB, int NB, int max_q_len, float scale, pa_dtype kv_dtype, void* workspace, size_t ws_bytes,
+                     int* dev_err, void* stream) {
     const NvtxRange nvtx_range("pa_prefill");
     g_msg[0] = 0;
     if (!kv_dtype_ok(kv_dtype)) return fail(PA_ERR_UNSUPPORTED, "kv_dtype must be F16 or BF16");
@@ -301,7 +307,8 @@ pa_status pa_prefill(void* out, pa_dtype out_dtype, const void* q, const void* p
     if ((long long)NB * B >= (1LL << 31)) return fail(PA_ERR_UNSUPPORTED, "NB * B must be < 2^31");
     if (T == 0 || max_q_len == 0) return PA_OK;
     if (!out || !q || !pool || !block_tables || !ctx_lens || !q_start) return fail(PA_ERR_INVALID, "null pointer");
-    if (!aligned16(out) || !aligned16(q) || !aligned16(pool)) return fail(PA_ERR_INVALID, "16-byte alignment");
+    if (!aligned16(out) || !aligned16(q) || !aligned16(pool) || !aligned16(workspace))
+        return fail(PA_ERR_INVALID, "16-byte alignment");
     if (out_dtype == PA_F32 && (reinterpret_cast<uintptr_t>(out) & 31u))
         return fail(PA_ERR_INVALID, "an fp32 out must be 32-byte aligned");
     PrefillArgs a;
@@ -323,6 +330,8 @@ pa_status pa_prefill(void* out, pa_dtype out_dtype, const void* q, const void* p
     a.max_q_len = max_q_len;
     a.scale = scale;
     a.kv_dtype = kv_dtype;
+    a.workspace = workspace;
+    a.ws_bytes = workspace ? ws_bytes : 0;
     a.dev_err = dev_err;
     a.stream = static_cast<cudaStream_t>(stream);
     return launch_prefill(a);

@@ -92,10 +92,20 @@ struct PrefillArgs {
     int N, T, H_q, H_kv, D, B, MB, NB, max_q_len;
     float scale;
     int kv_dtype;
+    void* workspace;  // nullable: V staging area for bf16 caches
+    size_t ws_bytes;
     int* dev_err;
     cudaStream_t stream;
 };
 
+struct PrefillWorkspace {
+    int S_pad;     // keys per staged (sequence, KV head) row: MB * B rounded up to the 128-key tile
+    size_t split;  // offset of the per-(sequence, KV head) marks (after the staged V)
+    size_t total;
+};
+
+// Returns false for invalid arguments.
+bool prefill_workspace_layout(int N, int H_kv, int D, int B, int MB, PrefillWorkspace* out);
 pa_status launch_prefill(const PrefillArgs& a);
 
 pa_status launch_partition_reduce(void* out, int out_dtype, const float* m2, const float* l, const float* acc,

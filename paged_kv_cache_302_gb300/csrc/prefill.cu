@@ -41,6 +41,7 @@ constexpr int kPfThreads = kPfSoftmaxThreads + 64;  // + warp 8: TMA, warp 9: MM
 constexpr int kPfStages = 2;     // K and V stages in shared memory
 constexpr uint32_t kTmemCols = 512;  // S/P of query tiles 0, 1 (128 columns each), then O_0, O_1 (D columns each)
 constexpr uint32_t kRegion = kPfRows * 128;  // one [128 rows][64 columns] 16-bit swizzled region: 16 KB
+constexpr int kGroupKeys = 32;               // keys per warp of the V staging kernel (one key tile per CTA)
 
 struct PrefillParams {
     const int32_t* tables;
@@ -51,6 +52,10 @@ struct PrefillParams {
     int out_dtype;
     float scale_log2;
     uint64_t wait_ns;  // limit of the hand-off waits (the exit path waits with kWaitLimitNs)
+    // bf16 V staged as fp16 by stage_v_kernel (null: V read from the pool, P split into two bf16 parts)
+    const void* vstage;
+    const int* vsplit;  // per (sequence, KV head): non-zero when a tile could not be staged exactly
+    int S_pad;          // keys per staged (sequence, KV head) row: a multiple of 128
     int* err;
 };
 
@@ -175,10 +180,81 @@ __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
     return d;
 }
 
+// Lane-wise unsigned maximum of two 16-bit pairs (PTX max.u16x2).
+__device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// A pair of bfloat16 values as a pair of IEEE binary16 values, round to nearest even (exact when each value is
+// zero or of magnitude in [2^-14, 65504]: a bfloat16 significand has 8 bits, a binary16 one 11).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
+}
+
+// ----------------------------------------------------------------------------- V staging (bf16 caches)
+
+// The value product takes P in fp16 (11-bit significand) when V is fp16.  A bf16 cache's V is staged as fp16 by
+// this kernel, per (sequence, KV head) in key order: stage[s * H_kv + h][t][D], t < S_pad, zeros past the context.
+// bf16 -> fp16 is exact for zero and for magnitudes in [2^-14, 65504].  A (sequence, KV head) row with a magnitude
+// of 65536 or more (fp16 would overflow; also inf and NaN), or with a 32-key group of context keys whose
+// magnitudes are all below 2^-10 (fp16 subnormals would drop bits), is marked in `split` (zeroed before this
+// kernel): the prefill kernel's CTAs of that row then read V from the pool and take P as a high and a low bf16
+// part (two products), as every CTA does when nothing is staged.  One CTA per 128-key tile and KV head, one warp
+// per 32 keys: lane i reads the 16-byte chunks i, i + 32, ... of its group's V rows (D * 2 / 16 chunks per row,
+// rows through the block table), so a warp load covers whole rows.
+template <int D>
+__global__ void __launch_bounds__(128) stage_v_kernel(const uint16_t* __restrict__ pool, const int32_t* __restrict__ tables,
+                                                      const int32_t* __restrict__ ctx_lens, int H_kv, int B, int MB,
+                                                      int NB, int S_pad, uint16_t* __restrict__ stage,
+                                                      int* __restrict__ split, int* err) {
+    constexpr int CPR = D * 2 / 16;  // 16-byte chunks per V row
+    griddep_wait();
+    griddep_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int s = blockIdx.z, h = blockIdx.y, tile = blockIdx.x;
+    const int t0 = tile * kPfKeys + (threadIdx.x >> 5) * kGroupKeys;
+    int ctx = ctx_lens[s];
+    if (ctx < 0 || ctx > MB * B) ctx = 0;  // flagged by the prefill kernel, which then computes nothing
+    if (tile * kPfKeys >= ctx) return;     // uniform per CTA: past the last key tile the prefill reads
+    uint4 x[CPR];
+    uint32_t mx = 0;
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < CPR; ++k) {
+        const int c = lane + 32 * k, t = t0 + c / CPR, q = c % CPR;
+        x[k] = make_uint4(0, 0, 0, 0);
+        if (t < ctx) {
+            const int blk = tables[(size_t)s * MB + t / B];
+            if ((unsigned)blk < (unsigned)NB) {
+                const uint16_t* row = pool + (((size_t)blk * B + t % B) * 2 + 1) * H_kv * D + (size_t)h * D;
+                x[k] = __ldg(reinterpret_cast<const uint4*>(row) + q);
+                mx = vmax_u16x2(mx, vmax_u16x2(vmax_u16x2(x[k].x & 0x7fff7fffu, x[k].y & 0x7fff7fffu),
+                                               vmax_u16x2(x[k].z & 0x7fff7fffu, x[k].w & 0x7fff7fffu)));
+            } else {
+                bad = true;
+            }
+        }
+    }
+    if (bad) flag_error(err, PA_DEV_ERR_BLOCK);
+    mx = __reduce_max_sync(0xffffffffu, max(mx & 0xffffu, mx >> 16));
+    // 0x4780: bf16 magnitude bits of 65536; 0x3a80: of 2^-10
+    if (lane == 0 && t0 < ctx && (mx >= 0x4780u || mx < 0x3a80u)) atomicOr(split + s * H_kv + h, 1);
+    uint4* dst = reinterpret_cast<uint4*>(stage + ((size_t)(s * H_kv + h) * S_pad + t0) * D);
+#pragma unroll
+    for (int k = 0; k < CPR; ++k)
+        dst[lane + 32 * k] = make_uint4(bf16x2_to_f16x2(x[k].x), bf16x2_to_f16x2(x[k].y), bf16x2_to_f16x2(x[k].z),
+                                        bf16x2_to_f16x2(x[k].w));
 }
 
 // ----------------------------------------------------------------------------- kernel
@@ -187,17 +263,25 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                 const __grid_constant__ CUtensorMap tm_kv,
                                                                 const __grid_constant__ CUtensorMap tm_kv_blk,
+                                                                const __grid_constant__ CUtensorMap tm_vs,
                                                                 const PrefillParams p) {
     constexpr int DH = D / 64;          // 64-column halves of a head row
     constexpr int NK = D / 16;          // k-steps of S = Q K^T
     constexpr int NT = kPfKeys / 16;    // k-steps of O += P V
     constexpr int NS = kPfStages;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-    // bf16 P (8-bit significand) would put the relative L2 error near 1e-3, so bf16 keeps P as a high and a low
-    // part (two value products); fp16 P (11 bits, ~1.4e-4) needs only the one
-    constexpr bool kSplitP = kBf16;
+    // The value product takes P in fp16 (11-bit significand, relative L2 error ~1.4e-4) when V is fp16: an fp16
+    // cache, or a bf16 cache whose V stage_v_kernel staged as fp16.  A CTA of a bf16 cache with nothing staged, or
+    // of a (sequence, KV head) row the staging kernel marked, reads V from the pool and takes P as a high and a low
+    // bf16 part, two products (a single bf16 P, 8 bits, would put the error near 1e-3).  The choice is made once per
+    // CTA, outside the loops: a choice per key tile inside them measured ~7 % slower (the issuing thread lost its
+    // straight-line code), one per 32 keys a quarter slower.
+    const bool staged = kBf16 && p.vstage != nullptr;
+    const bool split = kBf16 && (!staged || __ldg(p.vsplit + blockIdx.z * p.H_kv + blockIdx.y) != 0);
+    const bool vstaged = staged && !split;  // V tiles come from the staging area
     constexpr uint32_t idesc_s = umma_idesc(kBf16, kPfRows, kPfKeys, false);
-    constexpr uint32_t idesc_o = umma_idesc(kBf16, kPfRows, D, true);
+    constexpr uint32_t idesc_o16 = umma_idesc(false, kPfRows, D, true);
+    constexpr uint32_t idesc_obf = umma_idesc(true, kPfRows, D, true);
     constexpr uint32_t kTile = DH * kRegion;  // one Q tile (128 rows x D), or one K or V tile (128 keys x D)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -238,8 +322,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     auto ph = [](int j) { return (uint32_t)((j / NS) & 1); };
     // With B = 8 the K and V tiles are stored block by block, [block][half][8 rows][128 bytes], and one copy
     // brings a whole block; otherwise each tile holds one 128-key region per 64-column half, [half][128 rows][128 B]
-    // (one copy per block and half), which measured faster for the value product at B = 16 and 32.
-    const bool k_blk = p.B == 8, v_blk = p.B == 8;
+    // (one copy per block and half), which measured faster for the value product at B = 16 and 32.  A staged V
+    // tile always has the second layout.
+    const bool k_blk = p.B == 8, v_blk = p.B == 8 && !vstaged;
     const uint32_t blk_bytes = (uint32_t)DH * p.B * 128;
 
     if (warp == 0) {
@@ -312,6 +397,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                 if (!ok) break;
                 const uint32_t bar = (which ? vfull0 : kfull0) + 8 * b;
                 const uint32_t dst = (which ? sV0 : sK0) + b * kTile;
+                if (which && vstaged) {
+                    // the staged V tile: 128 keys of this (sequence, KV head), one copy per 64-column half
+                    if (lane == 0) {
+                        armed[1] = t + 1;
+                        mbar_arrive_expect_tx(bar, kTile);
+                        for (int dh = 0; dh < DH; ++dh)
+                            tma_load_4d(dst + dh * kRegion, &tm_vs, bar, 0, dh, t * kPfKeys, s * p.H_kv + g, pol);
+                    }
+                    __syncwarp();
+                    continue;
+                }
                 if (lane == 0) {
                     armed[which] = t + 1;  // expect_tx and every copy below, with no wait in between
                     mbar_arrive_expect_tx(bar, bytes);
@@ -349,17 +445,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             umma_commit(sfull0 + 8 * w);
             if (w == 1) umma_commit(kfree0 + 8 * st(j));  // K_j has served both query tiles
         };
-        auto issue_pv = [&](int w, int j) {  // O_w += P_hi V (+ P_lo V for bf16), P read from TMEM
+        // O_w += P V with P read from TMEM: one fp16 product per 16 keys, or (split) P_hi V + P_lo V in bf16
+        auto issue_pv = [&](int w, int j, auto split_c) {
             const uint32_t vb = sV0 + st(j) * kTile;
             const uint32_t pcol = tmem + (uint32_t)w * kPfKeys;
             const uint32_t ocol = tmem + 2 * kPfKeys + (uint32_t)w * D;
             const uint64_t dv = !v_blk ? umma_desc(vb, kRegion, 1024) : umma_desc(vb, 1024, blk_bytes);
             const uint32_t vstep = !v_blk ? (16 * 128) >> 4 : (2 * blk_bytes) >> 4;
+            constexpr bool kSplit = decltype(split_c)::value;
 #pragma unroll
             for (int ks = 0; ks < NT; ++ks) {
                 const uint64_t vdesc = dv + (uint64_t)(ks * vstep);
-                umma_f16_ta(ocol, pcol + ks * 8, vdesc, idesc_o, (j > 0 || ks > 0));
-                if (kSplitP) umma_f16_ta(ocol, pcol + kPfKeys / 2 + ks * 8, vdesc, idesc_o, 1u);
+                umma_f16_ta(ocol, pcol + ks * 8, vdesc, kSplit ? idesc_obf : idesc_o16, (j > 0 || ks > 0));
+                if (kSplit) umma_f16_ta(ocol, pcol + kPfKeys / 2 + ks * 8, vdesc, idesc_obf, 1u);
             }
             umma_commit(pvd0 + 8 * w);
             if (w == 1) umma_commit(vfree0 + 8 * st(j));
@@ -371,21 +469,29 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                 issue_s(0, 0);
                 issue_s(1, 0);
             }
-            for (int j = 0; j < ntiles && ok; ++j) {
-                const bool more = j + 1 < ntiles;
-                for (int w = 0; w < 2 && ok; ++w) {
-                    ok = waited(prd0 + 8 * w, (uint32_t)(j & 1)) && (w == 1 || waited(vfull0 + 8 * st(j), ph(j)));
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(w, j);
-                    if (more) {
-                        ok = (w == 1 || waited(kfull0 + 8 * st(j + 1), ph(j + 1))) &&
-                             waited(pvd0 + 8 * w, (uint32_t)(j & 1));
+            // the tile loop, one copy per kind of value product
+            auto tiles = [&](auto split_c) {
+                for (int j = 0; j < ntiles && ok; ++j) {
+                    const bool more = j + 1 < ntiles;
+                    for (int w = 0; w < 2 && ok; ++w) {
+                        ok = waited(prd0 + 8 * w, (uint32_t)(j & 1)) &&
+                             (w == 1 || waited(vfull0 + 8 * st(j), ph(j)));
+                        if (!ok) break;
                         tc_fence_after();
-                        if (ok) issue_s(w, j + 1);
+                        issue_pv(w, j, split_c);
+                        if (more) {
+                            ok = (w == 1 || waited(kfull0 + 8 * st(j + 1), ph(j + 1))) &&
+                                 waited(pvd0 + 8 * w, (uint32_t)(j & 1));
+                            tc_fence_after();
+                            if (ok) issue_s(w, j + 1);
+                        }
                     }
                 }
-            }
+            };
+            if (split)
+                tiles(std::true_type{});
+            else
+                tiles(std::false_type{});
             // arrives once every product issued above has completed (at once when none was issued)
             umma_commit(mmadone);
         }
@@ -451,26 +557,35 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             m_ref = m_new;
             const float m_use = m_new == NEG_INF ? 0.f : m_new;
             const float2 nm2 = make_float2(-m_use, -m_use);
-            // P overwrites S in TMEM: the high parts in the buffer's first 64 columns, the low parts after
+            // P overwrites S in TMEM: fp16 in the buffer's first 64 columns; split, the high bf16 parts there and
+            // the low parts in the next 64
             float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            auto write_p = [&](auto split_c) {
+                constexpr bool kSplit = decltype(split_c)::value;
+                using PT = typename std::conditional<kSplit, __nv_bfloat16, __half>::type;
 #pragma unroll
-            for (int c = 0; c < kPfKeys / 32; ++c) {
-                uint32_t hi[16], lo[16];
+                for (int c = 0; c < kPfKeys / 32; ++c) {
+                    uint32_t hi[16], lo[16];
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float2 x = ffma2(make_float2(v[32 * c + i], v[32 * c + i + 1]), sc2, nm2);
-                    x.x = fast_exp2(x.x);
-                    x.y = fast_exp2(x.y);
-                    ls[(i >> 1) & 1] = fadd2(ls[(i >> 1) & 1], x);
-                    hi[i / 2] = Mma<T>::pack(x.x, x.y);
-                    if (kSplitP) {
-                        const float2 f = fsub2(x, Mma<T>::unpack(hi[i / 2]));
-                        lo[i / 2] = Mma<T>::pack(f.x, f.y);
+                    for (int i = 0; i < 32; i += 2) {
+                        float2 x = ffma2(make_float2(v[32 * c + i], v[32 * c + i + 1]), sc2, nm2);
+                        x.x = fast_exp2(x.x);
+                        x.y = fast_exp2(x.y);
+                        ls[(i >> 1) & 1] = fadd2(ls[(i >> 1) & 1], x);
+                        hi[i / 2] = Mma<PT>::pack(x.x, x.y);
+                        if (kSplit) {
+                            const float2 f = fsub2(x, Mma<PT>::unpack(hi[i / 2]));
+                            lo[i / 2] = Mma<PT>::pack(f.x, f.y);
+                        }
                     }
+                    tmem_st16(t_s + c * 16, hi);
+                    if (kSplit) tmem_st16(t_s + kPfKeys / 2 + c * 16, lo);
                 }
-                tmem_st16(t_s + c * 16, hi);
-                if (kSplitP) tmem_st16(t_s + kPfKeys / 2 + c * 16, lo);
-            }
+            };
+            if (split)
+                write_p(std::true_type{});
+            else
+                write_p(std::false_type{});
             const float2 lsum = fadd2(ls[0], ls[1]);
             l = fmaf(l, alpha, lsum.x + lsum.y);
             // O_w is rescaled (rarely: only when the maximum grew by more than 2^8) once PV_w(j-1) has landed
@@ -489,7 +604,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             // V rows past the context may hold anything (even NaN): tile 0's warpgroup zeroes them before either
             // query tile's PV (PV_0 is issued first) can meet them with P = 0
             const int nvalid = min(kPfKeys, ctx - k0);
-            if (wg == 0 && nvalid < kPfKeys) {
+            if (wg == 0 && nvalid < kPfKeys && !vstaged) {  // a staged tile has zeros there already
                 ok = waited(vfull0 + 8 * st(j), ph(j)) && ok;
                 const uint32_t vb = sV0 + st(j) * kTile;
                 for (int rr = nvalid + (warp & 3); rr < kPfKeys; rr += 4)
@@ -587,9 +702,19 @@ static size_t prefill_smem_bytes(int D) {
     return 1024 + (size_t)(2 + 2 * kPfStages) * DH * kRegion + 256;  // Q[2], K[NS], V[NS], barriers
 }
 
+bool prefill_workspace_layout(int N, int H_kv, int D, int B, int MB, PrefillWorkspace* L) {
+    if (N <= 0 || H_kv <= 0 || (D != 64 && D != 128) || B <= 0 || MB <= 0) return false;
+    const long long keys = (long long)MB * B;
+    L->S_pad = (int)((keys + kPfKeys - 1) / kPfKeys * kPfKeys);
+    const size_t stage = (size_t)N * H_kv * L->S_pad * D * 2;
+    L->split = (stage + 255) & ~size_t(255);
+    L->total = L->split + (((size_t)N * H_kv * sizeof(int) + 255) & ~size_t(255));
+    return true;
+}
+
 template <typename T, int D>
 static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tkv,
-                             const CUtensorMap& tkv_blk) {
+                             const CUtensorMap& tkv_blk, const CUtensorMap& tvs, const PrefillWorkspace* ws) {
     auto kern = prefill_kernel<T, D>;
     const size_t smem = prefill_smem_bytes(D);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -611,9 +736,24 @@ static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const 
     p.out_dtype = a.out_dtype;
     p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
     p.wait_ns = wait_limit_ns();
+    p.vstage = ws ? a.workspace : nullptr;
+    int* vsplit = ws ? reinterpret_cast<int*>(static_cast<uint8_t*>(a.workspace) + ws->split) : nullptr;
+    p.vsplit = vsplit;
+    p.S_pad = ws ? ws->S_pad : 0;
     p.err = a.dev_err;
+    if (ws) {
+        // stage V as fp16 (before the prefill kernel, same stream); the rows it marks start unmarked
+        e = cudaMemsetAsync(vsplit, 0, sizeof(int) * (size_t)a.N * a.H_kv, a.stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (prefill workspace)");
+        e = launch_kernel(stage_v_kernel<D>, dim3(ws->S_pad / kPfKeys, a.H_kv, a.N), dim3(kPfKeys / kGroupKeys * 32), 0,
+                          a.stream,
+                          static_cast<const uint16_t*>(a.pool), a.tables, a.ctx_lens, a.H_kv, a.B, a.MB, a.NB,
+                          ws->S_pad, static_cast<uint16_t*>(a.workspace), vsplit, a.dev_err);
+        count_launch();
+        if (e != cudaSuccess) return cuda_fail(e, "V staging launch");
+    }
     const dim3 grid((a.max_q_len + 2 * p.TQ - 1) / (2 * p.TQ), a.H_kv, a.N);
-    e = launch_kernel(kern, grid, dim3(kPfThreads), smem, a.stream, tq, tkv, tkv_blk, p);
+    e = launch_kernel(kern, grid, dim3(kPfThreads), smem, a.stream, tq, tkv, tkv_blk, tvs, p);
     count_launch();
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "prefill launch");
 }
@@ -649,10 +789,30 @@ pa_status launch_prefill(const PrefillArgs& a) {
     r = fn(&tkv_blk, dt, 5, const_cast<void*>(a.pool), pd, ps, pb, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(pool blocks) failed (CUresult %d)", (int)r);
+    // staged V (bf16 caches with a workspace): [N * H_kv][S_pad][D] 16-bit; dims 64 columns, column half, key,
+    // (sequence, kv head); box = 128 keys of one half
+    CUtensorMap tvs;
+    std::memset(&tvs, 0, sizeof tvs);
+    PrefillWorkspace ws;
+    const bool use_ws = a.kv_dtype == PA_BF16 && a.workspace != nullptr;
+    if (use_ws) {
+        if (!prefill_workspace_layout(a.N, a.H_kv, a.D, a.B, a.MB, &ws))
+            return fail(PA_ERR_INVALID, "invalid prefill workspace arguments");
+        if (a.ws_bytes < ws.total) return fail(PA_ERR_INVALID, "prefill workspace too small: %zu < %zu", a.ws_bytes,
+                                               ws.total);
+        cuuint64_t vd[4] = {64, (cuuint64_t)DH, (cuuint64_t)ws.S_pad, (cuuint64_t)a.N * a.H_kv};
+        cuuint64_t vs[3] = {128, (cuuint64_t)a.D * 2, (cuuint64_t)ws.S_pad * a.D * 2};
+        cuuint32_t vb[4] = {64, 1, (cuuint32_t)kPfKeys, 1};
+        r = fn(&tvs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, a.workspace, vd, vs, vb, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(staged V) failed (CUresult %d)", (int)r);
+    }
+    const PrefillWorkspace* w = use_ws ? &ws : nullptr;
     if (a.kv_dtype == PA_BF16)
-        return a.D == 128 ? run_prefill<__nv_bfloat16, 128>(a, tq, tkv, tkv_blk)
-                          : run_prefill<__nv_bfloat16, 64>(a, tq, tkv, tkv_blk);
-    return a.D == 128 ? run_prefill<__half, 128>(a, tq, tkv, tkv_blk) : run_prefill<__half, 64>(a, tq, tkv, tkv_blk);
+        return a.D == 128 ? run_prefill<__nv_bfloat16, 128>(a, tq, tkv, tkv_blk, tvs, w)
+                          : run_prefill<__nv_bfloat16, 64>(a, tq, tkv, tkv_blk, tvs, w);
+    return a.D == 128 ? run_prefill<__half, 128>(a, tq, tkv, tkv_blk, tvs, w)
+                      : run_prefill<__half, 64>(a, tq, tkv, tkv_blk, tvs, w);
 }
 
 }  // namespace pa

@@ -50,13 +50,20 @@ def test_device_calls_reject_bad_arguments_before_touching_the_gpu():
     # pa_prefill: placeholder addresses are never dereferenced because validation fails first
     out, q, pool, tab, ctx, qs = 0x1010, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000
 
-    def prefill(out=out, out_dtype=2, B=16, scale=0.1):
-        return L.pa_prefill(out, out_dtype, q, pool, tab, ctx, qs, 1, 1, 8, 8, 128, B, 1, 1, 1, scale, 1, None, None)
+    def prefill(out=out, out_dtype=2, B=16, scale=0.1, ws=None):
+        return L.pa_prefill(out, out_dtype, q, pool, tab, ctx, qs, 1, 1, 8, 8, 128, B, 1, 1, 1, scale, 1, ws, 0,
+                            None, None)
 
     assert prefill() == pa.PA_ERR_INVALID and "32-byte" in pa.last_error()
     assert prefill(out=0x1008, out_dtype=1) == pa.PA_ERR_INVALID and "16-byte" in pa.last_error()
+    assert prefill(out=0x1020, ws=0x7008) == pa.PA_ERR_INVALID and "16-byte" in pa.last_error()
     assert prefill(out=0x1020, B=4) == pa.PA_ERR_UNSUPPORTED
     assert prefill(out=0x1020, scale=0.0) == pa.PA_ERR_INVALID
+    # the prefill workspace: staged V [N * H_kv][S_pad][D] 16-bit (S_pad = MB * B rounded up to 128 keys), then
+    # one flag byte per 32 keys, each part rounded up to 256 bytes
+    assert L.pa_prefill_workspace_bytes(2, 8, 128, 16, 10) == 2 * 8 * 256 * 128 * 2 + 256
+    assert L.pa_prefill_workspace_bytes(3, 1, 64, 8, 17) == 3 * 256 * 64 * 2 + 256
+    assert L.pa_prefill_workspace_bytes(0, 8, 128, 16, 10) == 0 and L.pa_prefill_workspace_bytes(1, 8, 96, 16, 1) == 0
 
 
 def _run_same_ops(NB, B, order, ops):

@@ -391,10 +391,12 @@ def test_no_call_writes_outside_its_buffers():
     qs_d.copy_(torch.from_numpy(q_start))
     q_big, q_d = _carved(qp.shape, torch.bfloat16)
     q_d.copy_(torch.from_numpy(qp.view(np.int16)).view(torch.bfloat16))
-    pa.pa_prefill(outp, q_d, cp.pool, pt_tab, pt_ctx, qs_d, max(chunks))
-    _margins_intact(out_big, qs_big, q_big)
+    pws_big, pws = _carved((pa.pa_prefill_workspace_bytes(wp.N, wp.H_kv, wp.D, wp.B, cp.MB),), torch.uint8)
     refp = oracle.paged_prefill(qp, cp.host_pool, cp.tables, cp.ctx, q_start, wp.dtype, nthreads=0)
-    C.assert_close(outp.cpu().numpy(), refp, "guarded prefill")
+    for stage_v in (True, False):            # V staged as fp16 in the workspace, and P split without one
+        pa.pa_prefill(outp, q_d, cp.pool, pt_tab, pt_ctx, qs_d, max(chunks), workspace=pws, stage_v=stage_v)
+        _margins_intact(out_big, qs_big, q_big, pws_big)
+        C.assert_close(outp.cpu().numpy(), refp, f"guarded prefill, stage_v={stage_v}")
 
 
 def test_block_relabelling_gives_identical_bits():

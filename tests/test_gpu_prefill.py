@@ -11,7 +11,7 @@ import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def _run(c, chunks, seed=0, out_dtype=torch.float32, rows=None):
+def _run(c, chunks, seed=0, out_dtype=torch.float32, rows=None, stage_v=True):
     w = c.w
     rng = np.random.default_rng(seed)
     q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
@@ -21,7 +21,7 @@ def _run(c, chunks, seed=0, out_dtype=torch.float32, rows=None):
     out = torch.full((T, w.H_q, w.D), float("nan"), dtype=out_dtype, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     pa.pa_prefill(out, C.to_dev(q, w.dtype), c.pool, tab, ctx, torch.from_numpy(q_start).cuda(), int(max(chunks)),
-                  dev_err=err)
+                  dev_err=err, stage_v=stage_v)
     torch.cuda.synchronize()
     assert err.item() == 0
     ref = oracle.paged_prefill(q, c.host_pool, c.tables, c.ctx, q_start, w.dtype, rows=rows, nthreads=0)
@@ -33,32 +33,35 @@ def _with_ctx(w, ctx):
     return w
 
 
+@pytest.mark.parametrize("stage_v", [True, False], ids=["staged_v", "split_p"])
 @pytest.mark.parametrize("chunks_of", ["full", "tail", "mixed"])
-def test_prefill_llama_shaped_every_output(chunks_of):
+def test_prefill_llama_shaped_every_output(chunks_of, stage_v):
     w = _with_ctx(W.llama3_8b(n_seqs=4), [200, 513, 77, 1000])
     c = C.build_paged(w)
     chunks = {"full": list(w.ctx), "tail": [1, 1, 1, 1], "mixed": [200, 130, 1, 257]}[chunks_of]
-    out, ref, _, _ = _run(c, chunks)
+    out, ref, _, _ = _run(c, chunks, stage_v=stage_v)
     C.assert_close(out.cpu().numpy(), ref, f"prefill {chunks_of}")
 
 
+@pytest.mark.parametrize("stage_v", [True, False], ids=["staged_v", "split_p"])
 @pytest.mark.parametrize("make,ctx,chunks", [
     (lambda: W.opt13b(n_seqs=3), [300, 129, 700], [300, 50, 129]),         # MHA, fp16
     (lambda: W.yi34b_long(n_seqs=2, ctx_len=600, B=8), [600, 331], [600, 200]),   # G = 7, B = 8
     (lambda: W.yi34b_long(n_seqs=2, ctx_len=600, B=32), [600, 331], [333, 331]),  # B = 32
 ])
-def test_prefill_group_sizes_and_block_sizes(make, ctx, chunks):
+def test_prefill_group_sizes_and_block_sizes(make, ctx, chunks, stage_v):
     c = C.build_paged(_with_ctx(make(), ctx))
-    out, ref, _, _ = _run(c, chunks)
+    out, ref, _, _ = _run(c, chunks, stage_v=stage_v)
     C.assert_close(out.cpu().numpy(), ref, f"prefill {c.w.name}")
 
 
-def test_prefill_head_dim_64():
-    w = W.Workload("d64", 1, 3, 8, 2, 64, 8, "f16", np.array([100, 9, 256], np.int32), 200,
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_prefill_head_dim_64(dtype):
+    w = W.Workload("d64", 1, 3, 8, 2, 64, 8, dtype, np.array([100, 9, 256], np.int32), 200,
                    np.random.default_rng(3).permutation(200).astype(np.int32))
     c = C.build_paged(w)
     out, ref, _, _ = _run(c, [100, 9, 129])
-    C.assert_close(out.cpu().numpy(), ref, "prefill D=64")
+    C.assert_close(out.cpu().numpy(), ref, f"prefill D=64 {dtype}")
 
 
 def test_prefill_one_token_chunks_match_decode():
@@ -125,3 +128,56 @@ def test_prefill_device_errors_are_flagged_not_faulted():
     assert err.item() & pa.PA_DEV_ERR_CTX
     out2, ref, _, _ = _run(c, chunks)
     C.assert_close(out2.cpu().numpy(), ref, "prefill after flagged calls")
+
+
+def _scale_v_bits(bits: np.ndarray, log2_factor: int) -> np.ndarray:
+    """bf16 bit patterns times 2^log2_factor (exact: only the exponent moves; zeros stay zero)."""
+    f = (bits.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** log2_factor)
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_prefill_workspace_too_small_is_refused():
+    w = _with_ctx(W.llama3_8b(n_seqs=2), [300, 129])
+    c = C.build_paged(w)
+    tab, ctx = c.dev_tables()
+    need = pa.pa_prefill_workspace_bytes(w.N, w.H_kv, w.D, w.B, c.MB)
+    q = torch.zeros((300, w.H_q, w.D), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((300, w.H_q, w.D), device="cuda")
+    qs = torch.tensor([0, 200, 300], dtype=torch.int32, device="cuda")
+    small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    launches = pa.launch_count()
+    with pytest.raises(pa.PAError, match="workspace too small"):
+        pa.pa_prefill(out, q, c.pool, tab, ctx, qs, 200, workspace=small)
+    assert pa.launch_count() == launches
+
+
+@pytest.mark.parametrize("stage_v", [True, False], ids=["staged_v", "split_p"])
+@pytest.mark.parametrize("B", [8, 16])
+def test_prefill_bf16_value_groups_outside_the_fp16_range(B, stage_v):
+    """bf16 V is staged as fp16 for the value product only where that is exact; a (sequence, KV head) with a V
+    magnitude >= 65536 (fp16 would overflow), or with a 32-key group whose values are all below 2^-10 (fp16
+    subnormals would drop bits), is computed from the pool with the split P instead.  Sequence 0: every V times
+    2^17; sequence 1: every V times 2^-20; sequence 2: one block of V times 2^17 among ordinary ones; sequence 3
+    ordinary (staged).  Each output row is checked against the oracle relative to its own magnitude."""
+    w = _with_ctx(W.yi34b_long(n_seqs=4, ctx_len=700, B=B), [700, 450, 600, 300])
+    c = C.build_paged(w)
+    host = c.host_pool
+    for s, (blocks, k) in enumerate([(None, 17), (None, -20), ([5], 17)]):
+        nb = -(-int(c.ctx[s]) // w.B)
+        ids = c.tables[s, :nb] if blocks is None else c.tables[s, blocks]
+        for b in ids:
+            host[b, :, 1] = _scale_v_bits(host[b, :, 1], k)
+    # unused slots of the last blocks were NaN-poisoned and scaled as NaN: NaN stays NaN
+    c.pool.copy_(C.to_dev(host, w.dtype).view(c.pool.shape))
+    chunks = [700, 300, 600, 300]
+    out, ref, _, q_start = _run(c, chunks, stage_v=stage_v)
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    for s in range(w.N):
+        g = got[q_start[s]:q_start[s + 1]].reshape(-1, w.D)
+        r = ref[q_start[s]:q_start[s + 1]].reshape(-1, w.D)
+        scale = np.maximum(np.abs(r).max(axis=1, keepdims=True), 1.0 if s != 1 else 1e-30)
+        d = np.abs(g - r) / scale
+        assert d.max() <= C.ATOL, f"seq {s}: max row-relative |diff| {d.max():.3e}"
+        rel = np.linalg.norm(g - r) / np.linalg.norm(r)
+        assert rel <= C.REL_L2, f"seq {s}: rel L2 {rel:.3e}"
