@@ -11,16 +11,22 @@
 // query tiles, which share every K/V tile it loads (320 threads):
 //   * warp 8 (TMA): both Q tiles once, then K and V of each 128-key tile into a
 //     two-stage ring, through the block table, 128-byte swizzled; lane b issues
-//     the copies of the tile's b-th KV block;
+//     the copies of the tile's b-th KV block (V of a staged bf16 cache: two
+//     boxes per tile from the staging area);
 //   * warp 9 (MMA, one thread): S_w = Q_w K^T as tcgen05.mma (M 128, N 128,
-//     K 16 steps) into TMEM columns [128w, 128w + 128), and O_w += P_hi V +
-//     P_lo V (bf16; fp16 needs only P V) with P read from those same TMEM columns (the A operand) and V an
-//     MN-major shared-memory operand; O_w sits in TMEM columns 256 + D w;
+//     K 16 steps) into TMEM columns [128w, 128w + 128), and O_w += P V with P
+//     read from those same TMEM columns (the A operand) and V an MN-major
+//     shared-memory operand; O_w sits in TMEM columns 256 + D w;
 //   * warps 0-3 and 4-7 (softmax, one warpgroup per query tile): every thread
 //     owns one TMEM lane = one query row; it reads its S row with tcgen05.ld,
 //     masks causally, keeps the running maximum (rescaling O only when the
 //     maximum grows by more than 2^8), and writes the probabilities back over S
-//     as a high and a low 16-bit part for bf16, one fp16 part for fp16 (tcgen05.st).
+//     (tcgen05.st).
+// The value product is one fp16 product per 16 keys (P in fp16) when V is fp16:
+// an fp16 cache, or a bf16 cache whose V stage_v_kernel has staged as fp16 in
+// the caller's workspace.  Otherwise (a bf16 cache without a workspace, or a
+// row whose values fp16 cannot hold exactly) P is a high and a low bf16 part
+// and the product is P_hi V + P_lo V.
 // Hand-offs are mbarriers; every wait is bounded.  Finally every thread reads
 // its O row, divides by its exponential sum and stores the row.
 #include <cuda.h>
@@ -210,51 +216,83 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // of 65536 or more (fp16 would overflow; also inf and NaN), or with a 32-key group of context keys whose
 // magnitudes are all below 2^-10 (fp16 subnormals would drop bits), is marked in `split` (zeroed before this
 // kernel): the prefill kernel's CTAs of that row then read V from the pool and take P as a high and a low bf16
-// part (two products), as every CTA does when nothing is staged.  One CTA per 128-key tile and KV head, one warp
-// per 32 keys: lane i reads the 16-byte chunks i, i + 32, ... of its group's V rows (D * 2 / 16 chunks per row,
-// rows through the block table), so a warp load covers whole rows.
+// part (two products), as every CTA does when nothing is staged.
+// One CTA per 32 keys of a sequence and group of up to 8 KV heads.  One TMA box per KV block brings the block's V
+// rows of those heads into shared memory ([head][column half][token][64 columns], unswizzled; heads past H_kv
+// read as zeros), then the 256 threads convert 16-byte chunks and write whole 256-byte rows of the staging area.
+// (Plain loads through the block table, a warp per head, moved ~2.5 TB/s; the attention kernel's TMA boxes over
+// the same per-head rows move ~6.8 TB/s.)
+constexpr int kStageThreads = 256;
+constexpr int kStageHeads = 8;  // KV heads per CTA, one TMA box per KV block
+
 template <int D>
-__global__ void __launch_bounds__(128) stage_v_kernel(const uint16_t* __restrict__ pool, const int32_t* __restrict__ tables,
-                                                      const int32_t* __restrict__ ctx_lens, int H_kv, int B, int MB,
-                                                      int NB, int S_pad, uint16_t* __restrict__ stage,
-                                                      int* __restrict__ split, int* err) {
-    constexpr int CPR = D * 2 / 16;  // 16-byte chunks per V row
+__global__ void __launch_bounds__(kStageThreads) stage_v_kernel(const __grid_constant__ CUtensorMap tm_v,
+                                                                const int32_t* __restrict__ tables,
+                                                                const int32_t* __restrict__ ctx_lens, int H_kv,
+                                                                int B, int MB, int NB, int S_pad,
+                                                                uint16_t* __restrict__ stage,
+                                                                int* __restrict__ split, uint64_t wait_ns, int* err) {
+    constexpr int DH = D / 64;
+    constexpr int kRowChunks = DH * 8;  // 16-byte chunks per V row
+    extern __shared__ __align__(128) uint8_t vbuf[];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t hmax[kStageHeads];
     griddep_wait();
     griddep_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    const int s = blockIdx.z, h = blockIdx.y, tile = blockIdx.x;
-    const int t0 = tile * kPfKeys + (threadIdx.x >> 5) * kGroupKeys;
+    const int tid = threadIdx.x;
+    const int s = blockIdx.z, h0 = blockIdx.y * kStageHeads, t0 = blockIdx.x * kGroupKeys;
+    const int hb = min(kStageHeads, H_kv), nh = min(hb, H_kv - h0);
     int ctx = ctx_lens[s];
     if (ctx < 0 || ctx > MB * B) ctx = 0;  // flagged by the prefill kernel, which then computes nothing
-    if (tile * kPfKeys >= ctx) return;     // uniform per CTA: past the last key tile the prefill reads
-    uint4 x[CPR];
-    uint32_t mx = 0;
-    bool bad = false;
-#pragma unroll
-    for (int k = 0; k < CPR; ++k) {
-        const int c = lane + 32 * k, t = t0 + c / CPR, q = c % CPR;
-        x[k] = make_uint4(0, 0, 0, 0);
-        if (t < ctx) {
-            const int blk = tables[(size_t)s * MB + t / B];
-            if ((unsigned)blk < (unsigned)NB) {
-                const uint16_t* row = pool + (((size_t)blk * B + t % B) * 2 + 1) * H_kv * D + (size_t)h * D;
-                x[k] = __ldg(reinterpret_cast<const uint4*>(row) + q);
-                mx = vmax_u16x2(mx, vmax_u16x2(vmax_u16x2(x[k].x & 0x7fff7fffu, x[k].y & 0x7fff7fffu),
-                                               vmax_u16x2(x[k].z & 0x7fff7fffu, x[k].w & 0x7fff7fffu)));
-            } else {
-                bad = true;
+    if (t0 >= (ctx + kPfKeys - 1) / kPfKeys * kPfKeys) return;  // uniform per CTA: past the last key tile read
+    const int nvalid = max(0, min(kGroupKeys, ctx - t0));
+    const int nblk = (nvalid + B - 1) / B;  // KV blocks holding this CTA's context keys
+    const uint32_t box_bytes = 128u * B * DH * hb;
+    const uint32_t bar_s = smem_addr(&bar), buf_s = smem_addr(vbuf);
+    if (tid < kStageHeads) hmax[tid] = 0;
+    if (tid == 0) {
+        mbar_init(bar_s, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar_s, nblk * box_bytes);
+        const uint64_t pol = policy_evict_first();
+        for (int b = 0; b < nblk; ++b) {
+            int e = tables[(size_t)s * MB + t0 / B + b];
+            if ((unsigned)e >= (unsigned)NB) {
+                flag_error(err, PA_DEV_ERR_BLOCK);
+                e = NB;  // past the tensor: TMA fills zeros
             }
+            tma_load_5d(buf_s + b * box_bytes, &tm_v, bar_s, 0, e * B, 0, h0, 1, pol);
         }
     }
-    if (bad) flag_error(err, PA_DEV_ERR_BLOCK);
-    mx = __reduce_max_sync(0xffffffffu, max(mx & 0xffffu, mx >> 16));
+    if (!mbar_wait_bounded(bar_s, 0, nullptr, wait_ns)) {
+        if (tid == 0) flag_error(err, PA_DEV_ERR_TIMEOUT);
+        mbar_wait_bounded(bar_s, 0, nullptr);  // the copies land in this CTA's shared memory: let them
+    }
+    // chunk c: row (key tt = (c / kRowChunks) % 32, head hh = c / (kRowChunks * 32)), column chunk c % kRowChunks;
+    // with 256 threads every pass over the chunks covers a single head
+    constexpr int kPerHead = kRowChunks * kGroupKeys;
+    for (int c = tid; c < hb * kPerHead; c += kStageThreads) {
+        const int hh = c / kPerHead, tt = (c / kRowChunks) % kGroupKeys, q = c % kRowChunks;
+        const int half = q / 8, cq = q % 8;
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if (tt < nvalid)
+            x = *reinterpret_cast<const uint4*>(vbuf + (tt / B) * box_bytes +
+                                                (((hh * DH + half) * B + tt % B) * 128 + cq * 16));
+        uint32_t m = vmax_u16x2(vmax_u16x2(x.x & 0x7fff7fffu, x.y & 0x7fff7fffu),
+                                vmax_u16x2(x.z & 0x7fff7fffu, x.w & 0x7fff7fffu));
+        m = __reduce_max_sync(0xffffffffu, max(m & 0xffffu, m >> 16));
+        if ((tid & 31) == 0) atomicMax(&hmax[hh], m);
+        if (hh < nh)
+            reinterpret_cast<uint4*>(stage + ((size_t)(s * H_kv + h0 + hh) * S_pad + t0 + tt) * D)[q] =
+                make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
+    }
+    __syncthreads();
     // 0x4780: bf16 magnitude bits of 65536; 0x3a80: of 2^-10
-    if (lane == 0 && t0 < ctx && (mx >= 0x4780u || mx < 0x3a80u)) atomicOr(split + s * H_kv + h, 1);
-    uint4* dst = reinterpret_cast<uint4*>(stage + ((size_t)(s * H_kv + h) * S_pad + t0) * D);
-#pragma unroll
-    for (int k = 0; k < CPR; ++k)
-        dst[lane + 32 * k] = make_uint4(bf16x2_to_f16x2(x[k].x), bf16x2_to_f16x2(x[k].y), bf16x2_to_f16x2(x[k].z),
-                                        bf16x2_to_f16x2(x[k].w));
+    if (tid < nh && nvalid > 0 && (hmax[tid] >= 0x4780u || hmax[tid] < 0x3a80u))
+        atomicOr(split + s * H_kv + h0 + tid, 1);
 }
 
 // ----------------------------------------------------------------------------- kernel
@@ -511,118 +549,122 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         const float NEG_INF = -INFINITY;
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
         float m_ref = NEG_INF, l = 0.f;
-        for (int j = 0; j < ntiles; ++j) {
-            const int k0 = j * kPfKeys;
-            ok = waited(sfull0 + 8 * wg, (uint32_t)(j & 1)) && ok;
-            tc_fence_after();
-            float v[kPfKeys];
-            {
-                uint32_t* u = reinterpret_cast<uint32_t*>(v);
-#pragma unroll
-                for (int c = 0; c < kPfKeys / 32; ++c)
-                    asm volatile(
-                        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
-                        "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
-                        "[%32];"
-                        : "=r"(u[32 * c + 0]), "=r"(u[32 * c + 1]), "=r"(u[32 * c + 2]), "=r"(u[32 * c + 3]),
-                          "=r"(u[32 * c + 4]), "=r"(u[32 * c + 5]), "=r"(u[32 * c + 6]), "=r"(u[32 * c + 7]),
-                          "=r"(u[32 * c + 8]), "=r"(u[32 * c + 9]), "=r"(u[32 * c + 10]), "=r"(u[32 * c + 11]),
-                          "=r"(u[32 * c + 12]), "=r"(u[32 * c + 13]), "=r"(u[32 * c + 14]), "=r"(u[32 * c + 15]),
-                          "=r"(u[32 * c + 16]), "=r"(u[32 * c + 17]), "=r"(u[32 * c + 18]), "=r"(u[32 * c + 19]),
-                          "=r"(u[32 * c + 20]), "=r"(u[32 * c + 21]), "=r"(u[32 * c + 22]), "=r"(u[32 * c + 23]),
-                          "=r"(u[32 * c + 24]), "=r"(u[32 * c + 25]), "=r"(u[32 * c + 26]), "=r"(u[32 * c + 27]),
-                          "=r"(u[32 * c + 28]), "=r"(u[32 * c + 29]), "=r"(u[32 * c + 30]), "=r"(u[32 * c + 31])
-                        : "r"(t_s + c * 32)
-                        : "memory");
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            }
-            // only tiles that reach past the tile's first position need the causal mask
-            const bool masked = k0 + kPfKeys - 1 > first_pos || !row_ok;
-            if (masked) {
-#pragma unroll
-                for (int i = 0; i < kPfKeys; ++i) v[i] = k0 + i <= qpos ? v[i] : NEG_INF;
-            }
-            float mx[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
-#pragma unroll
-            for (int i = 0; i < kPfKeys; i += 8) {
-                mx[0] = fmax3(mx[0], v[i], v[i + 1]);
-                mx[1] = fmax3(mx[1], v[i + 2], v[i + 3]);
-                mx[2] = fmax3(mx[2], v[i + 4], v[i + 5]);
-                mx[3] = fmax3(mx[3], v[i + 6], v[i + 7]);
-            }
-            const float m_tile = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * p.scale_log2;
-            float m_new = m_ref;
-            if (j == 0 || m_tile > m_ref + 8.f) m_new = fmaxf(m_ref, m_tile);
-            const float alpha = (j == 0 || m_new == m_ref) ? 1.f : fast_exp2(m_ref - m_new);
-            m_ref = m_new;
-            const float m_use = m_new == NEG_INF ? 0.f : m_new;
-            const float2 nm2 = make_float2(-m_use, -m_use);
-            // P overwrites S in TMEM: fp16 in the buffer's first 64 columns; split, the high bf16 parts there and
-            // the low parts in the next 64
-            float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            auto write_p = [&](auto split_c) {
-                constexpr bool kSplit = decltype(split_c)::value;
-                using PT = typename std::conditional<kSplit, __nv_bfloat16, __half>::type;
-#pragma unroll
-                for (int c = 0; c < kPfKeys / 32; ++c) {
-                    uint32_t hi[16], lo[16];
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float2 x = ffma2(make_float2(v[32 * c + i], v[32 * c + i + 1]), sc2, nm2);
-                        x.x = fast_exp2(x.x);
-                        x.y = fast_exp2(x.y);
-                        ls[(i >> 1) & 1] = fadd2(ls[(i >> 1) & 1], x);
-                        hi[i / 2] = Mma<PT>::pack(x.x, x.y);
-                        if (kSplit) {
-                            const float2 f = fsub2(x, Mma<PT>::unpack(hi[i / 2]));
-                            lo[i / 2] = Mma<PT>::pack(f.x, f.y);
-                        }
-                    }
-                    tmem_st16(t_s + c * 16, hi);
-                    if (kSplit) tmem_st16(t_s + kPfKeys / 2 + c * 16, lo);
-                }
-            };
-            if (split)
-                write_p(std::true_type{});
-            else
-                write_p(std::false_type{});
-            const float2 lsum = fadd2(ls[0], ls[1]);
-            l = fmaf(l, alpha, lsum.x + lsum.y);
-            // O_w is rescaled (rarely: only when the maximum grew by more than 2^8) once PV_w(j-1) has landed
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                ok = waited(pvd0 + 8 * wg, (uint32_t)((j - 1) & 1)) && ok;
+        // the tile loop, one copy per kind of value product (the choice is made once, outside it)
+        auto tiles = [&](auto split_c) {
+            for (int j = 0; j < ntiles; ++j) {
+                const int k0 = j * kPfKeys;
+                ok = waited(sfull0 + 8 * wg, (uint32_t)(j & 1)) && ok;
                 tc_fence_after();
+                float v[kPfKeys];
+                {
+                    uint32_t* u = reinterpret_cast<uint32_t*>(v);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    float o[32];
-                    tmem_ld32(t_o + c * 32, o);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                    tmem_st32(t_o + c * 32, o);
+                    for (int c = 0; c < kPfKeys / 32; ++c)
+                        asm volatile(
+                            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+                            "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+                            "%28, %29, %30, %31}, [%32];"
+                            : "=r"(u[32 * c + 0]), "=r"(u[32 * c + 1]), "=r"(u[32 * c + 2]), "=r"(u[32 * c + 3]),
+                              "=r"(u[32 * c + 4]), "=r"(u[32 * c + 5]), "=r"(u[32 * c + 6]), "=r"(u[32 * c + 7]),
+                              "=r"(u[32 * c + 8]), "=r"(u[32 * c + 9]), "=r"(u[32 * c + 10]), "=r"(u[32 * c + 11]),
+                              "=r"(u[32 * c + 12]), "=r"(u[32 * c + 13]), "=r"(u[32 * c + 14]), "=r"(u[32 * c + 15]),
+                              "=r"(u[32 * c + 16]), "=r"(u[32 * c + 17]), "=r"(u[32 * c + 18]), "=r"(u[32 * c + 19]),
+                              "=r"(u[32 * c + 20]), "=r"(u[32 * c + 21]), "=r"(u[32 * c + 22]), "=r"(u[32 * c + 23]),
+                              "=r"(u[32 * c + 24]), "=r"(u[32 * c + 25]), "=r"(u[32 * c + 26]), "=r"(u[32 * c + 27]),
+                              "=r"(u[32 * c + 28]), "=r"(u[32 * c + 29]), "=r"(u[32 * c + 30]), "=r"(u[32 * c + 31])
+                            : "r"(t_s + c * 32)
+                            : "memory");
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                 }
+                // only tiles that reach past the tile's first position need the causal mask
+                const bool masked = k0 + kPfKeys - 1 > first_pos || !row_ok;
+                if (masked) {
+#pragma unroll
+                    for (int i = 0; i < kPfKeys; ++i) v[i] = k0 + i <= qpos ? v[i] : NEG_INF;
+                }
+                float mx[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+#pragma unroll
+                for (int i = 0; i < kPfKeys; i += 8) {
+                    mx[0] = fmax3(mx[0], v[i], v[i + 1]);
+                    mx[1] = fmax3(mx[1], v[i + 2], v[i + 3]);
+                    mx[2] = fmax3(mx[2], v[i + 4], v[i + 5]);
+                    mx[3] = fmax3(mx[3], v[i + 6], v[i + 7]);
+                }
+                const float m_tile = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * p.scale_log2;
+                float m_new = m_ref;
+                if (j == 0 || m_tile > m_ref + 8.f) m_new = fmaxf(m_ref, m_tile);
+                const float alpha = (j == 0 || m_new == m_ref) ? 1.f : fast_exp2(m_ref - m_new);
+                m_ref = m_new;
+                const float m_use = m_new == NEG_INF ? 0.f : m_new;
+                const float2 nm2 = make_float2(-m_use, -m_use);
+                // P overwrites S in TMEM: fp16 in the buffer's first 64 columns; split, the high bf16 parts there and
+                // the low parts in the next 64
+                float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                auto write_p = [&](auto split_c) {
+                    constexpr bool kSplit = decltype(split_c)::value;
+                    using PT = typename std::conditional<kSplit, __nv_bfloat16, __half>::type;
+#pragma unroll
+                    for (int c = 0; c < kPfKeys / 32; ++c) {
+                        uint32_t hi[16], lo[16];
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            float2 x = ffma2(make_float2(v[32 * c + i], v[32 * c + i + 1]), sc2, nm2);
+                            x.x = fast_exp2(x.x);
+                            x.y = fast_exp2(x.y);
+                            ls[(i >> 1) & 1] = fadd2(ls[(i >> 1) & 1], x);
+                            hi[i / 2] = Mma<PT>::pack(x.x, x.y);
+                            if (kSplit) {
+                                const float2 f = fsub2(x, Mma<PT>::unpack(hi[i / 2]));
+                                lo[i / 2] = Mma<PT>::pack(f.x, f.y);
+                            }
+                        }
+                        tmem_st16(t_s + c * 16, hi);
+                        if (kSplit) tmem_st16(t_s + kPfKeys / 2 + c * 16, lo);
+                    }
+                };
+                write_p(split_c);
+                const float2 lsum = fadd2(ls[0], ls[1]);
+                l = fmaf(l, alpha, lsum.x + lsum.y);
+                // O_w is rescaled (rarely: only when the maximum grew by more than 2^8) once PV_w(j-1) has landed
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    ok = waited(pvd0 + 8 * wg, (uint32_t)((j - 1) & 1)) && ok;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(t_o + c * 32, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tmem_st32(t_o + c * 32, o);
+                    }
+                }
+                // V rows past the context may hold anything (even NaN): tile 0's warpgroup zeroes them before either
+                // query tile's PV (PV_0 is issued first) can meet them with P = 0
+                const int nvalid = min(kPfKeys, ctx - k0);
+                if (wg == 0 && nvalid < kPfKeys && !vstaged) {  // a staged tile has zeros there already
+                    ok = waited(vfull0 + 8 * st(j), ph(j)) && ok;
+                    const uint32_t vb = sV0 + st(j) * kTile;
+                    for (int rr = nvalid + (warp & 3); rr < kPfKeys; rr += 4)
+                        for (int dh = 0; dh < DH; ++dh)
+                            if (lane < 8)
+                                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
+                                                 v_blk ? vb + (uint32_t)(rr / p.B) * blk_bytes +
+                                                             (uint32_t)(dh * p.B + rr % p.B) * 128 + lane * 16
+                                                       : vb + dh * kRegion + rr * 128 + lane * 16),
+                                             "r"(0)
+                                             : "memory");
+                }
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(prd0 + 8 * wg);
+                if (*abort_flag) break;
             }
-            // V rows past the context may hold anything (even NaN): tile 0's warpgroup zeroes them before either
-            // query tile's PV (PV_0 is issued first) can meet them with P = 0
-            const int nvalid = min(kPfKeys, ctx - k0);
-            if (wg == 0 && nvalid < kPfKeys && !vstaged) {  // a staged tile has zeros there already
-                ok = waited(vfull0 + 8 * st(j), ph(j)) && ok;
-                const uint32_t vb = sV0 + st(j) * kTile;
-                for (int rr = nvalid + (warp & 3); rr < kPfKeys; rr += 4)
-                    for (int dh = 0; dh < DH; ++dh)
-                        if (lane < 8)
-                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
-                                             v_blk ? vb + (uint32_t)(rr / p.B) * blk_bytes +
-                                                         (uint32_t)(dh * p.B + rr % p.B) * 128 + lane * 16
-                                                   : vb + dh * kRegion + rr * 128 + lane * 16),
-                                         "r"(0)
-                                         : "memory");
-            }
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(prd0 + 8 * wg);
-            if (*abort_flag) break;
-        }
+        };
+        if (split)
+            tiles(std::true_type{});
+        else
+            tiles(std::false_type{});
         const int jl = ntiles - 1;
         if (ok) ok = waited(pvd0 + 8 * wg, (uint32_t)(jl & 1));
         ok = __all_sync(0xffffffffu, ok);
@@ -714,7 +756,8 @@ bool prefill_workspace_layout(int N, int H_kv, int D, int B, int MB, PrefillWork
 
 template <typename T, int D>
 static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tkv,
-                             const CUtensorMap& tkv_blk, const CUtensorMap& tvs, const PrefillWorkspace* ws) {
+                             const CUtensorMap& tkv_blk, const CUtensorMap& tvs, const CUtensorMap* tvall,
+                             const PrefillWorkspace* ws) {
     auto kern = prefill_kernel<T, D>;
     const size_t smem = prefill_smem_bytes(D);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -745,10 +788,14 @@ static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const 
         // stage V as fp16 (before the prefill kernel, same stream); the rows it marks start unmarked
         e = cudaMemsetAsync(vsplit, 0, sizeof(int) * (size_t)a.N * a.H_kv, a.stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (prefill workspace)");
-        e = launch_kernel(stage_v_kernel<D>, dim3(ws->S_pad / kPfKeys, a.H_kv, a.N), dim3(kPfKeys / kGroupKeys * 32), 0,
-                          a.stream,
-                          static_cast<const uint16_t*>(a.pool), a.tables, a.ctx_lens, a.H_kv, a.B, a.MB, a.NB,
-                          ws->S_pad, static_cast<uint16_t*>(a.workspace), vsplit, a.dev_err);
+        const int hb = std::min(kStageHeads, a.H_kv);
+        const size_t vsmem = (size_t)kGroupKeys * D * 2 * hb;
+        e = cudaFuncSetAttribute(stage_v_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)vsmem);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(stage_v)");
+        const dim3 sgrid(ws->S_pad / kGroupKeys, (a.H_kv + kStageHeads - 1) / kStageHeads, a.N);
+        e = launch_kernel(stage_v_kernel<D>, sgrid, dim3(kStageThreads), vsmem, a.stream, *tvall, a.tables,
+                          a.ctx_lens, a.H_kv, a.B, a.MB, a.NB, ws->S_pad, static_cast<uint16_t*>(a.workspace), vsplit,
+                          p.wait_ns, a.dev_err);
         count_launch();
         if (e != cudaSuccess) return cuda_fail(e, "V staging launch");
     }
@@ -805,14 +852,25 @@ pa_status launch_prefill(const PrefillArgs& a) {
         cuuint32_t vb[4] = {64, 1, (cuuint32_t)kPfKeys, 1};
         r = fn(&tvs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, a.workspace, vd, vs, vb, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(staged V) failed (CUresult %d)", (int)r);
+        if (r != CUDA_SUCCESS)
+            return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(staged V) failed (CUresult %d)", (int)r);
+    }
+    // the pool's V rows of up to kStageHeads KV heads of one block, unswizzled, for the staging kernel
+    CUtensorMap tvall;
+    std::memset(&tvall, 0, sizeof tvall);
+    if (use_ws) {
+        cuuint32_t vb[5] = {64, (cuuint32_t)a.B, (cuuint32_t)DH, (cuuint32_t)std::min(kStageHeads, a.H_kv), 1};
+        r = fn(&tvall, dt, 5, const_cast<void*>(a.pool), pd, ps, vb, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(pool V rows) failed (CUresult %d)", (int)r);
     }
     const PrefillWorkspace* w = use_ws ? &ws : nullptr;
     if (a.kv_dtype == PA_BF16)
-        return a.D == 128 ? run_prefill<__nv_bfloat16, 128>(a, tq, tkv, tkv_blk, tvs, w)
-                          : run_prefill<__nv_bfloat16, 64>(a, tq, tkv, tkv_blk, tvs, w);
-    return a.D == 128 ? run_prefill<__half, 128>(a, tq, tkv, tkv_blk, tvs, w)
-                      : run_prefill<__half, 64>(a, tq, tkv, tkv_blk, tvs, w);
+        return a.D == 128 ? run_prefill<__nv_bfloat16, 128>(a, tq, tkv, tkv_blk, tvs, &tvall, w)
+                          : run_prefill<__nv_bfloat16, 64>(a, tq, tkv, tkv_blk, tvs, &tvall, w);
+    return a.D == 128 ? run_prefill<__half, 128>(a, tq, tkv, tkv_blk, tvs, &tvall, w)
+                      : run_prefill<__half, 64>(a, tq, tkv, tkv_blk, tvs, &tvall, w);
 }
 
 }  // namespace pa
