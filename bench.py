@@ -429,9 +429,10 @@ def run_ours(args):
     traffic, traffic_note = profile_traffic(att_bytes)
 
     # ---- end-to-end through the public API with host buffers
-    e2e_value, h2d, d2h = None, 0, 0
+    e2e_value, h2d, d2h, e2e_parts = None, 0, 0, None
     if not args.no_e2e:
-        e2e_value, h2d, d2h = run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world, tab)
+        e2e_value, h2d, d2h, e2e_parts = run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world,
+                                                 tab)
 
     # ---- CPU baseline (rank 0, N = 1 only)
     cpu = None
@@ -465,7 +466,8 @@ def run_ours(args):
                          "bytes_per_launch": att_bytes, "per_unit": f"{per_tok} B per context token",
                          "peak_source": peak_src, "traffic_note": traffic_note},
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "breakdown": e2e_parts},
             "gpu_launches": launches,
             "clocks": clk.summary(),
             **extra,
@@ -480,12 +482,16 @@ def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world, tab
     """Decode steps through the public API from pinned host buffers.  Each step's inputs (q and the new K/V) sit in
     a pinned staging buffer of their own; the host block allocation of the step (slots, lengths and block-table
     updates, padded to a fixed count with skipped rows) is written into the same buffer.  Inside the timed region,
-    per step: the host allocation of the NEXT step (it needs only the lengths, so it runs while the device works)
-    and one CUDA graph launch that copies the staging buffer host->device, applies the table updates, writes the
-    cache and runs the decode (plan, attention, merge) with its output in pinned host memory, so the kernels write
-    the result rows across the host link themselves (the step's device->host bytes); then a synchronisation.
-    The graphs hold the same library calls a user would make eagerly, captured once per staging buffer before
-    the timed region: they remove the host launch latency, not device work."""
+    per step i: the host allocation of step i+1 (it needs only the lengths, so it runs while the device works on
+    step i), then the host->device copy of step i+1's staging buffer on a copy stream (into the device staging
+    buffer step i-1 used: the host synchronised with step i-1 before), so that it overlaps step i's kernels as a
+    serving loop's double-buffered inputs would; then one CUDA graph launch for step i (applies the table updates,
+    writes the cache and runs the decode -- plan, attention, merge -- with its output in pinned host memory, so
+    the kernels write the result rows across the host link themselves: the step's device->host bytes), after
+    the main stream waits for step i's copy; then a synchronisation.  Every timed step still moves its own input
+    and output bytes.  The graphs hold the same library calls a user would make eagerly, captured once per device
+    staging buffer before the timed region: they remove the host launch latency, not device work.  Returns the
+    e2e rate, the bytes in and out per step, and a breakdown of one step's costs measured after the timed region."""
     import torch
 
     import paged_kv_cache_302_gb300 as pa
@@ -517,27 +523,31 @@ def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world, tab
         hb[o_k:o_k + nk] = k.view(np.uint8).reshape(-1)
         hb[o_v:o_v + nk] = v.view(np.uint8).reshape(-1)
         stage.append(h)
-    d_stage = torch.empty(total, dtype=torch.uint8, device=dev)
-    d_q = d_stage[:nq].view(torch.bfloat16).view(w.N, w.H_q, w.D)
-    d_k = d_stage[o_k:o_k + nk].view(torch.bfloat16).view(w.N, w.H_kv, w.D)
-    d_v = d_stage[o_v:o_v + nk].view(torch.bfloat16).view(w.N, w.H_kv, w.D)
-    d_slot = d_stage[o_s:o_s + w.N * 8].view(torch.int64)
-    d_ctx = d_stage[o_c:o_c + w.N * 4].view(torch.int32)
-    d_upd = d_stage[o_u:o_u + cap_u * 12].view(torch.int32).view(cap_u, 3)
+    main = torch.cuda.current_stream()
+    copy_stream = torch.cuda.Stream()
+    d_stages = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
     h_out = torch.empty((w.N, w.H_q, w.D), dtype=torch.float32).pin_memory()
     d2h = h_out.numel() * 4
-    e2e_bytes = []
+
+    def views(d):
+        return (d[:nq].view(torch.bfloat16).view(w.N, w.H_q, w.D),
+                d[o_k:o_k + nk].view(torch.bfloat16).view(w.N, w.H_kv, w.D),
+                d[o_v:o_v + nk].view(torch.bfloat16).view(w.N, w.H_kv, w.D),
+                d[o_s:o_s + w.N * 8].view(torch.int64),
+                d[o_c:o_c + w.N * 4].view(torch.int32),
+                d[o_u:o_u + cap_u * 12].view(torch.int32).view(cap_u, 3))
 
     graphs = []
-    for i in range(nsteps):
+    for d in d_stages:
+        d_q, d_k, d_v, d_slot, d_ctx, d_upd = views(d)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            d_stage.copy_(stage[i], non_blocking=True)
             pa.pa_update_block_tables(tab, d_upd, dev_err=err)
             pa.pa_reshape_and_cache(d_k, d_v, pool, d_slot, dev_err=err)
             pa.pa_decode(h_out, d_q, pool, tab, d_ctx, max_ctx, partition_tokens=pt, workspace=ws, dev_err=err)
         graphs.append(g)
     torch.cuda.synchronize()
+    copied = [torch.cuda.Event() for _ in range(2)]
 
     def prepare(i):
         """Host block allocation of step i into its staging buffer (it needs the lengths only)."""
@@ -552,78 +562,74 @@ def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world, tab
         hb[o_u:o_u + cap_u * 12] = u.view(np.uint8).reshape(-1)
         return pairs, int(ctx.astype(np.int64).sum()) * per_tok
 
+    def copy_in(i):
+        """Host->device copy of step i's staging buffer on the copy stream (device buffer i % 2)."""
+        with torch.cuda.stream(copy_stream):
+            d_stages[i % 2].copy_(stage[i], non_blocking=True)
+            copied[i % 2].record(copy_stream)
+
     def e2e_step(i, prep, next_i):
-        """Runs step i; the host prepares step next_i while the device works."""
+        """Runs step i; the host prepares and copies in step next_i while the device works."""
         pairs, nbytes = prep
+        main.wait_event(copied[i % 2])
         if pairs.size:   # copy-on-write before the step's cache write (none in this workload: no forks)
             pa.pa_copy_blocks(pool, torch.from_numpy(pairs).to(dev), dev_err=err)
-        graphs[i].replay()
-        nxt = prepare(next_i) if next_i is not None else None
-        torch.cuda.current_stream().synchronize()
+        graphs[i % 2].replay()
+        nxt = None
+        if next_i is not None:
+            nxt = prepare(next_i)
+            copy_in(next_i)
+        main.synchronize()
         return nbytes, nxt
 
     prep = prepare(0)
+    copy_in(0)
     for i in range(args.warmup):
         _, prep = e2e_step(i, prep, i + 1)
     if world > 1:
         torch.distributed.barrier()
+    e2e_bytes = []
     t0 = time.perf_counter()
     for i in range(args.warmup, nsteps):
         nbytes, prep = e2e_step(i, prep, i + 1 if i + 1 < nsteps else None)
         e2e_bytes.append(nbytes)
     t_e2e = time.perf_counter() - t0
+    copy_stream.synchronize()
     assert int(err.item()) == 0, f"device error flags {int(err.item())}"
     # the last step's result, as the kernels wrote it into host memory, against the same decode into device memory
+    last = (nsteps - 1) % 2
+    d_q, _, _, _, d_ctx, _ = views(d_stages[last])
     pa.pa_decode(out, d_q, pool, tab, d_ctx, max_ctx, partition_tokens=pt, workspace=ws, dev_err=err)
     assert torch.equal(out.cpu(), h_out), "decode output written to host memory differs from the device result"
+
+    # breakdown of one step, measured apart (each piece alone, so they do not add up to the pipelined step):
+    # the host allocation, the input copy and the step's graph (device time, output into host memory)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    reps = 10
+    ev[0].record(main)
+    for _ in range(reps):
+        d_stages[last].copy_(stage[nsteps - 1], non_blocking=True)
+    ev[1].record(main)
+    for _ in range(reps):
+        graphs[last].replay()     # replays the last step: it rewrites its own token and reads its own lengths
+    ev[2].record(main)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), h_out), "replayed step differs"
+    probe = pa.BlockAllocator.from_state(alloc.export_state())
+    th = time.perf_counter()
+    for _ in range(reps):
+        probe.append_batch(seq_ids, ones, table_updates=True)
+    t_host = (time.perf_counter() - th) / reps
+    probe.close()
+    breakdown = {"host_allocation_us": t_host * 1e6,
+                 "input_copy_us": ev[0].elapsed_time(ev[1]) * 1e3 / reps,
+                 "device_step_us": ev[1].elapsed_time(ev[2]) * 1e3 / reps,
+                 "step_us": t_e2e / e2e_steps * 1e6,
+                 "note": "each piece timed alone after the timed region; in the timed steps the host allocation and "
+                         "the input copy of step i+1 overlap the device work of step i"}
     t_e2e, e2e_total = whole_job(t_e2e, sum(e2e_bytes), dev)
     e2e_value = e2e_total / t_e2e / 1e9
-    return e2e_value, total, d2h
-
-
-def run_swap(args):
-    """Swap bandwidth: pa_swap_blocks moving whole Llama-3-8B-shaped blocks (16 tokens x 8 KV heads x 128, bf16:
-    64 KB each) between the device pool and a pinned host pool, both directions, CUDA events."""
-    import torch
-
-    import paged_kv_cache_302_gb300 as pa
-
-    torch.cuda.set_device(0)
-    B, H, D, nblk = 16, 8, 128, 4096            # 256 MB per direction
-    dev_pool = torch.empty((nblk, B, 2, H, D), dtype=torch.bfloat16, device="cuda").normal_()
-    host_pool = torch.empty((nblk, B, 2, H, D), dtype=torch.bfloat16).pin_memory()
-    rng = np.random.default_rng(12)
-    out_pairs = torch.from_numpy(np.stack([rng.permutation(nblk), rng.permutation(nblk)], 1).astype(np.int64)).cuda()
-    in_pairs = torch.from_numpy(np.stack([rng.permutation(nblk), rng.permutation(nblk)], 1).astype(np.int64)).cuda()
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    res = {}
-    for name, dst, src, pairs in (("swap_out_d2h", host_pool, dev_pool, out_pairs),
-                                  ("swap_in_h2d", dev_pool, host_pool, in_pairs)):
-        for _ in range(args.warmup):
-            pa.pa_swap_blocks(dst, src, pairs, dev_err=err)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
-            pa.pa_swap_blocks(dst, src, pairs, dev_err=err)
-        e1.record()
-        torch.cuda.synchronize()
-        t = e0.elapsed_time(e1) * 1e-3 / args.steps
-        res[name] = dev_pool.numel() * 2 / t / 1e9
-    # copy-engine reference: one contiguous cudaMemcpy of the same bytes each way
-    for name, dst, src in (("memcpy_d2h_contiguous", host_pool, dev_pool), ("memcpy_h2d_contiguous", dev_pool,
-                                                                             host_pool)):
-        dst.copy_(src, non_blocking=True)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
-            dst.copy_(src, non_blocking=True)
-        e1.record()
-        torch.cuda.synchronize()
-        res[name] = dev_pool.numel() * 2 / (e0.elapsed_time(e1) * 1e-3 / args.steps) / 1e9
-    assert int(err.item()) == 0
-    print(json.dumps({"measure": "pa_swap_blocks", "unit": "GB/s", "blocks": nblk, "block_bytes": B * 2 * H * D * 2,
-                      "steps": args.steps, **res}), flush=True)
-    return 0
+    return e2e_value, total, d2h, breakdown
 
 
 def measure_prefill(steps: int = 10, warmup: int = 3) -> list:
