@@ -4,6 +4,8 @@ Bit-exact: cache writes, block copies, allocator tables and slots.
 Attention outputs (fp32): max |diff| <= 2e-3 and relative L2 <= 1e-3.
 Every case, the full-size workloads included, compares every output row.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -218,6 +220,14 @@ def _schedule_view(ws, N, maxrec):
     return b[off: off + 16 * total].view(np.int32).reshape(total, 4), b[256: 256 + 4 * N].view(np.int32).copy()
 
 
+def _default_partition() -> int:
+    """The partition length partition_tokens=0 stands for: 512, or PA_DECODE_PARTITION when that names a positive
+    multiple of the 32-token stage (the library reads the variable once per process)."""
+    v = os.environ.get("PA_DECODE_PARTITION", "")
+    x = int(v) if v.strip().lstrip("-").isdigit() else 0
+    return x if x > 0 and x % 32 == 0 else 512
+
+
 @pytest.mark.parametrize("N,H_kv,pt,max_len", [(1, 8, 0, 3000), (33, 8, 0, 3000), (256, 8, 0, 8192),
                                                  (5000, 2, 64, 200), (40000, 1, -1, 700), (200000, 1, 32, 60)],
                          ids=["1", "33", "256", "5000-pt64", "40000-whole", "200000-pt32"])
@@ -229,7 +239,7 @@ def test_schedule_covers_every_work_item_once_longest_first(N, H_kv, pt, max_len
     the oracle (the tables point into a small shared pool, so sequences share blocks)."""
     rng = np.random.default_rng(N)
     B, D, H_q, NB = 16, 64, 2 * H_kv, 64
-    PT = {0: 512, -1: 1 << 30}.get(pt, pt)
+    PT = {0: _default_partition(), -1: 1 << 30}.get(pt, pt)
     ctx = rng.integers(1, max_len + 1, size=N).astype(np.int32)
     ctx[0] = max_len
     MB = (max_len + B - 1) // B

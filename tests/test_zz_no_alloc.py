@@ -23,17 +23,20 @@ import workloads as W
 pytestmark = pytest.mark.gpu
 
 
+PT = 512  # partition length of every call here (explicit: PA_DECODE_PARTITION may change the default)
+
+
 def _setup(w):
     c = C.build_paged(w, check_pool=False)
     tab, ctx = c.dev_tables()
     max_ctx = int(c.ctx.max())
-    assert pa.pa_decode_workspace_bytes(w.N, w.H_q, w.H_kv, w.D, max_ctx, 0) <= pa.PA_STATIC_WORKSPACE_BYTES
+    assert pa.pa_decode_workspace_bytes(w.N, w.H_q, w.H_kv, w.D, max_ctx, PT) <= pa.PA_STATIC_WORKSPACE_BYTES
     qd = C.to_dev(c.q, w.dtype)
-    ws = torch.empty(pa.pa_decode_workspace_bytes(w.N, w.H_q, w.H_kv, w.D, max_ctx, 0), dtype=torch.uint8,
+    ws = torch.empty(pa.pa_decode_workspace_bytes(w.N, w.H_q, w.H_kv, w.D, max_ctx, PT), dtype=torch.uint8,
                      device="cuda")
     ws.view(torch.int32).fill_(0x7FC00000)          # NaN in every float slot, an absurd value in every int slot
     ref = torch.full((w.N, w.H_q, w.D), float("nan"), device="cuda")
-    pa.pa_decode(ref, qd, c.pool, tab, ctx, max_ctx, workspace=ws)
+    pa.pa_decode(ref, qd, c.pool, tab, ctx, max_ctx, partition_tokens=PT, workspace=ws)
     torch.cuda.synchronize()
     C.assert_close(ref.cpu().numpy(), C.oracle_decode(c), f"pa_decode {w.name}")
     return c, tab, ctx, max_ctx, qd, ref
@@ -47,7 +50,7 @@ def test_no_alloc_matches_pa_decode_bit_for_bit_across_batches():
     for name in ("long", "long", "small", "small", "long"):
         c, tab, ctx, max_ctx, qd, ref = cases[name]
         out = torch.full_like(ref, float("nan"))
-        pa.pa_decode_no_alloc(out, qd, c.pool, tab, ctx, max_ctx, dev_err=err)
+        pa.pa_decode_no_alloc(out, qd, c.pool, tab, ctx, max_ctx, partition_tokens=PT, dev_err=err)
         torch.cuda.synchronize()
         assert err.item() == 0, f"{name}: device error flags {err.item()}"
         assert torch.equal(out, ref), f"{name}: pa_decode_no_alloc differs from pa_decode"
