@@ -17,8 +17,10 @@ Output: one JSON line (rank 0).  `value` is KV-read GB/s over whole steps;
 The same line carries, under `workloads`, the other decode workloads (OPT-13B,
 the copy-on-write parallel-sampling step, the 32K Yi-34B context paged at three
 block sizes and in the contiguous layout), the cache write and the block copy
-timed on their own, and the tensor-core prefill (about a second each;
-`--no-workloads` skips them).
+timed on their own (`cache_ops`), the tensor-core prefill, the block swap to
+and from pinned host memory (`swap`) and the virtually contiguous KV buffers
+(`vmm`: page mapping cost, decode over the mapped pages); about a second each,
+`--no-workloads` skips them.
 """
 from __future__ import annotations
 
@@ -451,7 +453,7 @@ def run_ours(args):
     extra = {}
     if rank == 0 and world == 1 and not args.no_workloads:
         extra = {"workloads": measure_workloads(hbm), "cache_ops": measure_cache_ops(hbm),
-                 "prefill": measure_prefill()}
+                 "prefill": measure_prefill(), "swap": measure_swap(), "vmm": measure_vmm()}
 
     if rank == 0:
         line = {
@@ -630,6 +632,57 @@ def run_e2e(args, w, alloc, pool, ws, out, err, MB, max_ctx, pt, dev, world, tab
     t_e2e, e2e_total = whole_job(t_e2e, sum(e2e_bytes), dev)
     e2e_value = e2e_total / t_e2e / 1e9
     return e2e_value, total, d2h, breakdown
+
+
+def measure_swap(steps: int = 10, warmup: int = 3) -> dict:
+    """Swap bandwidth: pa_swap_blocks moving whole Llama-3-8B-shaped blocks (16 tokens x 8 KV heads x 128, bf16:
+    64 KB each) between the device pool and a pinned host pool, both directions, CUDA events; and one contiguous
+    copy of the same bytes each way by the copy engine, for reference."""
+    import torch
+
+    import paged_kv_cache_302_gb300 as pa
+
+    B, H, D, nblk = 16, 8, 128, 4096            # 256 MB per direction
+    dev_pool = torch.empty((nblk, B, 2, H, D), dtype=torch.bfloat16, device="cuda").normal_()
+    host_pool = torch.empty((nblk, B, 2, H, D), dtype=torch.bfloat16).pin_memory()
+    rng = np.random.default_rng(12)
+    out_pairs = torch.from_numpy(np.stack([rng.permutation(nblk), rng.permutation(nblk)], 1).astype(np.int64)).cuda()
+    in_pairs = torch.from_numpy(np.stack([rng.permutation(nblk), rng.permutation(nblk)], 1).astype(np.int64)).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    res = {"unit": "GB/s", "blocks": nblk, "block_bytes": B * 2 * H * D * 2, "calls": steps}
+    for name, dst, src, pairs in (("swap_out_d2h", host_pool, dev_pool, out_pairs),
+                                  ("swap_in_h2d", dev_pool, host_pool, in_pairs)):
+        for _ in range(warmup):
+            pa.pa_swap_blocks(dst, src, pairs, dev_err=err)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            pa.pa_swap_blocks(dst, src, pairs, dev_err=err)
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) * 1e-3 / steps
+        res[name] = dev_pool.numel() * 2 / t / 1e9
+    for name, dst, src in (("memcpy_d2h_contiguous", host_pool, dev_pool), ("memcpy_h2d_contiguous", dev_pool,
+                                                                             host_pool)):
+        dst.copy_(src, non_blocking=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = dev_pool.numel() * 2 / (e0.elapsed_time(e1) * 1e-3 / steps) / 1e9
+    assert int(err.item()) == 0
+    del dev_pool, host_pool
+    return res
+
+
+def run_swap(args):
+    import torch
+
+    torch.cuda.set_device(0)
+    print(json.dumps({"measure": "pa_swap_blocks", **measure_swap(args.steps, args.warmup)}), flush=True)
+    return 0
 
 
 def measure_prefill(steps: int = 10, warmup: int = 3) -> list:
@@ -923,8 +976,8 @@ def measure_cache_ops(hbm: float) -> dict:
 
 
 def run_configs(args):
-    """The other workloads, the cache ops and the prefill, one JSON line each (the default run embeds the same
-    figures in its line)."""
+    """The other workloads, the cache ops, the prefill, the swap and the virtually contiguous KV, one JSON line each
+    (the default run embeds the same figures in its line)."""
     import torch
 
     torch.cuda.set_device(0)
@@ -934,17 +987,18 @@ def run_configs(args):
     print(json.dumps({"measure": "cache_ops", **measure_cache_ops(hbm)}), flush=True)
     for r in measure_prefill():
         print(json.dumps({"measure": "pa_prefill", **r}), flush=True)
+    print(json.dumps({"measure": "pa_swap_blocks", **measure_swap()}), flush=True)
+    print(json.dumps({"measure": "vkv", **measure_vmm()}), flush=True)
     return 0
 
 
-def run_vmm(args):
-    """Virtually contiguous KV: time to map physical pages on demand (per 2 MB page, create + map + access)
-    and decode over the mapped buffers, Yi-34B-shaped 8 x 32K context."""
+def measure_vmm() -> dict:
+    """Virtually contiguous KV: time to map physical pages on demand (per 2 MB page, create + map + access) and
+    decode over the mapped buffers, Yi-34B-shaped 8 x 32K context."""
     import torch
 
     import paged_kv_cache_302_gb300 as pa
 
-    torch.cuda.set_device(0)
     N, ctx_len, H_q, H_kv, D = 8, 32768, 56, 8, 128
     V = pa.VirtualKV(1, N, ctx_len, H_kv, D)
     reqs = [V.alloc_reqid() for _ in range(N)]
@@ -971,11 +1025,19 @@ def run_vmm(args):
     assert int(err.item()) == 0
     nbytes = N * ctx_len * 2 * H_kv * D * 2
     hbm, _ = peaks()
-    print(json.dumps({"measure": "vkv", "page_bytes": V.page_bytes, "pages_mapped": pages,
-                      "us_per_page_create_map_access": t_map / pages * 1e6, "decode_attend_gbs": nbytes / ta / 1e9,
-                      "decode_attend_frac_of_hbm": nbytes / ta / 1e9 / hbm, "tokens_per_page_per_buffer":
-                      V.page_bytes // (H_kv * D * 2)}), flush=True)
+    res = {"page_bytes": V.page_bytes, "pages_mapped": pages, "us_per_page_create_map_access": t_map / pages * 1e6,
+           "decode_step_gbs": nbytes / t / 1e9, "decode_attend_gbs": nbytes / ta / 1e9,
+           "decode_attend_frac_of_hbm": nbytes / ta / 1e9 / hbm,
+           "tokens_per_page_per_buffer": V.page_bytes // (H_kv * D * 2)}
     V.close()
+    return res
+
+
+def run_vmm(args):
+    import torch
+
+    torch.cuda.set_device(0)
+    print(json.dumps({"measure": "vkv", **measure_vmm()}), flush=True)
     return 0
 
 

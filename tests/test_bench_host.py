@@ -69,3 +69,16 @@ def test_attention_source_hash_spans_the_attention_kernel():
     import hashlib
     assert h == hashlib.sha256((src[a:e] + open(b.DEVICE_HDR).read()).encode()).hexdigest()
     assert h != hashlib.sha256(open(b.DEVICE_HDR).read().encode()).hexdigest()
+
+
+def test_every_measure_choice_has_its_function():
+    """Each --measure choice and each leg of the default line resolves to a function (a missing one would only
+    surface on a GPU machine)."""
+    b = _bench()
+    import inspect
+    src = inspect.getsource(b.main)
+    for name in ("run_ours", "run_reference", "run_swap", "run_prefill", "run_configs", "run_vmm", "measure_swap",
+                 "measure_vmm", "measure_prefill", "measure_workloads", "measure_cache_ops", "run_e2e"):
+        assert callable(getattr(b, name, None)), name
+    for choice in ("swap", "prefill", "configs", "vmm"):
+        assert f'"{choice}"' in src
