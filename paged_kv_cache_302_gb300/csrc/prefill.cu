@@ -47,7 +47,7 @@ constexpr int kPfThreads = kPfSoftmaxThreads + 64;  // + warp 8: TMA, warp 9: MM
 constexpr int kPfStages = 2;     // K and V stages in shared memory
 constexpr uint32_t kTmemCols = 512;  // S/P of query tiles 0, 1 (128 columns each), then O_0, O_1 (D columns each)
 constexpr uint32_t kRegion = kPfRows * 128;  // one [128 rows][64 columns] 16-bit swizzled region: 16 KB
-constexpr int kGroupKeys = 32;               // keys per warp of the V staging kernel (one key tile per CTA)
+constexpr int kGroupKeys = 32;               // keys per CTA of the V staging kernel (and per range-checked group)
 
 struct PrefillParams {
     const int32_t* tables;
@@ -60,7 +60,7 @@ struct PrefillParams {
     uint64_t wait_ns;  // limit of the hand-off waits (the exit path waits with kWaitLimitNs)
     // bf16 V staged as fp16 by stage_v_kernel (null: V read from the pool, P split into two bf16 parts)
     const void* vstage;
-    const int* vsplit;  // per (sequence, KV head): non-zero when a tile could not be staged exactly
+    const int* vsplit;  // per (sequence, KV head): non-zero when its V could not be staged exactly
     int S_pad;          // keys per staged (sequence, KV head) row: a multiple of 128
     int* err;
 };
