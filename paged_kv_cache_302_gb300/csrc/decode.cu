@@ -891,24 +891,52 @@ __global__ void __launch_bounds__(kReduceWarps * 32) partition_reduce_wide_kerne
     const float* lr = l + (size_t)r * P;
     const float* ar = acc + (size_t)r * P * D + lane * V;
     const int mine_n = np > warp ? (np - warp + kReduceWarps - 1) / kReduceWarps : 0;  // partitions of this warp
-    float M = -INFINITY;
-    for (int j = lane; j < mine_n; j += 32) M = fmaxf(M, mr[warp + kReduceWarps * j]);
-#pragma unroll
-    for (int k = 16; k > 0; k >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, k));
-    float o[V], den = 0.f;
+    // as the one-warp merge: every load of up to kMergeChunk of this warp's partitions first, then the sums
+    float M = -INFINITY, den = 0.f, o[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) o[v] = 0.f;
-    for (int base = 0; base < mine_n; base += 32) {
-        const int j = base + lane, pj = warp + kReduceWarps * j;
-        const float w = j < mine_n ? fast_exp2(mr[pj] - M) : 0.f;
-        if (j < mine_n) den += w * lr[pj];
-        const int n = min(32, mine_n - base);
-#pragma unroll 8
-        for (int jj = 0; jj < n; ++jj) {
-            const float wj = __shfl_sync(0xffffffffu, w, jj);
-            const float* a = ar + (size_t)(warp + kReduceWarps * (base + jj)) * D;
+    for (int base = 0; base < mine_n; base += kMergeChunk) {
+        const int n = min(kMergeChunk, mine_n - base);
+        const int pl = warp + kReduceWarps * (base + lane);
+        const float mv = lane < n ? mr[pl] : -INFINITY;
+        const float lv = lane < n ? lr[pl] : 0.f;
+        float a[kMergeChunk][V];
 #pragma unroll
-            for (int v = 0; v < V; ++v) o[v] += wj * a[v];
+        for (int j = 0; j < kMergeChunk; ++j) {
+            const float* src = ar + (size_t)(warp + kReduceWarps * (base + j)) * D;
+            if (j < n) {
+                if constexpr (V == 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(src);
+                    a[j][0] = x.x;
+                    a[j][1] = x.y;
+                    a[j][2] = x.z;
+                    a[j][3] = x.w;
+                } else {
+                    const float2 x = *reinterpret_cast<const float2*>(src);
+                    a[j][0] = x.x;
+                    a[j][1] = x.y;
+                }
+            } else {
+#pragma unroll
+                for (int v = 0; v < V; ++v) a[j][v] = 0.f;
+            }
+        }
+        float mc = mv;
+#pragma unroll
+        for (int k = 16; k > 0; k >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, k));
+        const float Mn = fmaxf(M, mc);
+        const float f = fast_exp2(M - Mn);  // 0 on the first chunk (M = -inf)
+        den *= f;
+#pragma unroll
+        for (int v = 0; v < V; ++v) o[v] *= f;
+        M = Mn;
+        const float w = lane < n ? fast_exp2(mv - Mn) : 0.f;
+        den += w * lv;
+#pragma unroll
+        for (int j = 0; j < kMergeChunk; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, w, j);
+#pragma unroll
+            for (int v = 0; v < V; ++v) o[v] += wj * a[j][v];
         }
     }
 #pragma unroll
