@@ -32,6 +32,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <type_traits>
@@ -48,6 +49,8 @@ constexpr int kPfStages = 2;     // K and V stages in shared memory
 constexpr uint32_t kTmemCols = 512;  // S/P of query tiles 0, 1 (128 columns each), then O_0, O_1 (D columns each)
 constexpr uint32_t kRegion = kPfRows * 128;  // one [128 rows][64 columns] 16-bit swizzled region: 16 KB
 constexpr int kGroupKeys = 32;               // keys per CTA of the V staging kernel (and per range-checked group)
+constexpr int kWKeys = 256;                  // keys per tile of prefill_wide_kernel (tcgen05 N of its S)
+constexpr int kStagePad = kWKeys;            // staged rows are written (zeros past the context) to a multiple of this
 
 struct PrefillParams {
     const int32_t* tables;
@@ -61,7 +64,9 @@ struct PrefillParams {
     // bf16 V staged as fp16 by stage_v_kernel (null: V read from the pool, P split into two bf16 parts)
     const void* vstage;
     const int* vsplit;  // per (sequence, KV head): non-zero when its V could not be staged exactly
-    int S_pad;          // keys per staged (sequence, KV head) row: a multiple of 128
+    int S_pad;          // keys per staged (sequence, KV head) row: a multiple of kStagePad
+    int only_split;     // prefill_kernel: serve only the rows marked in vsplit (prefill_wide_kernel takes the rest)
+    int max_q_len;      // longest chunk: prefill_wide_kernel's units per (sequence, KV head)
     int* err;
 };
 
@@ -244,7 +249,7 @@ __global__ void __launch_bounds__(kStageThreads) stage_v_kernel(const __grid_con
     const int hb = min(kStageHeads, H_kv), nh = min(hb, H_kv - h0);
     int ctx = ctx_lens[s];
     if (ctx < 0 || ctx > MB * B) ctx = 0;  // flagged by the prefill kernel, which then computes nothing
-    if (t0 >= (ctx + kPfKeys - 1) / kPfKeys * kPfKeys) return;  // uniform per CTA: past the last key tile read
+    if (t0 >= (ctx + kStagePad - 1) / kStagePad * kStagePad) return;  // uniform per CTA: past the last tile read
     const int nvalid = max(0, min(kGroupKeys, ctx - t0));
     const int nblk = (nvalid + B - 1) / B;  // KV blocks holding this CTA's context keys
     const uint32_t box_bytes = 128u * B * DH * hb;
@@ -314,9 +319,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     // bf16 part, two products (a single bf16 P, 8 bits, would put the error near 1e-3).  The choice is made once per
     // CTA, outside the loops: a choice per key tile inside them measured ~7 % slower (the issuing thread lost its
     // straight-line code), one per 32 keys a quarter slower.
-    const bool staged = kBf16 && p.vstage != nullptr;
-    const bool split = kBf16 && (!staged || __ldg(p.vsplit + blockIdx.z * p.H_kv + blockIdx.y) != 0);
-    const bool vstaged = staged && !split;  // V tiles come from the staging area
     constexpr uint32_t idesc_s = umma_idesc(kBf16, kPfRows, kPfKeys, false);
     constexpr uint32_t idesc_o16 = umma_idesc(false, kPfRows, D, true);
     constexpr uint32_t idesc_obf = umma_idesc(true, kPfRows, D, true);
@@ -340,6 +342,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 
     griddep_wait();
     griddep_launch_dependents();
+    // the marks are written by the staging kernel launched just before: read them only after the wait above
+    const bool staged = kBf16 && p.vstage != nullptr;
+    const bool split = kBf16 && (!staged || p.vsplit[blockIdx.z * p.H_kv + blockIdx.y] != 0);
+    const bool vstaged = staged && !split;  // V tiles come from the staging area
+    if (p.only_split && !split) return;     // uniform per CTA, before any allocation
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = blockIdx.z, g = blockIdx.y;
     const int qs = p.q_start[s], q_len = p.q_start[s + 1] - qs;
@@ -719,6 +726,507 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     }
 }
 
+// ----------------------------------------------------------------------------- one query tile, 256-key tiles
+
+// prefill_wide_kernel: the same computation for the rows whose value product takes P in fp16 (an fp16 cache, or a
+// bf16 cache's rows that stage_v_kernel converted; the rows it marked are left to prefill_kernel).  A unit of work
+// is one 128-row query tile of one (sequence, KV head).  S = Q K^T of 256 keys at once: a tcgen05.mma of N = 256 per
+// 16 columns of the head dim runs the tensor core at its full rate, where N = 128 products chained into one
+// accumulator (prefill_kernel's) ran at ~60 % of it.  S sits in TMEM columns [0, 256) and P (fp16) in columns of
+// its own, [384, 512), so the S product of the next key tile is issued as soon as the softmax has read S into
+// registers and runs while the exponentials are computed; O += P V (16 keys per product, O in columns
+// [256, 256 + D)) follows once P is written.
+// The kernel is persistent: one CTA per SM takes units c, c + grid, c + 2 grid, ... (ordered as wide_unit states),
+// so the set-up (TMEM, barriers) is paid once.  Between units the next query tile is loaded while the softmax works on the
+// last key tile, and the next unit's first S product runs while the softmax writes out the last unit's O.
+// Barrier phases follow counters that run across units (units, key tiles, ring items of the CTA).
+//   * warps 0-7 (softmax): warp w owns TMEM lanes 32 (w % 4) .. + 31 (query rows) and key columns 128 (w / 4) ..
+//     + 127 of each tile; the two warps of a row share their row maxima through shared memory when either grew, so
+//     both halves of P have one scale, and at the end their exponential sums; each stores D / 2 columns of O;
+//   * warp 8 (TMA): Q, then the K and V tiles into a ring of three 256-key slots in the order the products consume
+//     them (per unit: K_0, then K_{j+1}, V_j, ..., then the last V).  A slot is laid out [8-row group][column half]
+//     [8 rows][128 B], so one copy brings a whole KV block (both column halves of its B rows): lane b issues the
+//     copy of the tile's b-th block; a staged V tile is two copies of 128 keys;
+//   * warp 9 (MMA, one thread): per unit S_0, then S_{j+1} once the softmax has read S_j and PV_j once P_j is
+//     written.
+constexpr int kWSlots = 3;                   // ring slots, each one 256-key K or V tile
+constexpr uint32_t kWRegion = kWKeys * 128;  // 256 rows of 64 16-bit columns: 32 KB per column half
+constexpr uint32_t kWColO = 256;             // TMEM columns of O (D of them)
+constexpr uint32_t kWColP = 384;             // TMEM columns of P: 256 keys of fp16, two per column
+constexpr int kWBars = 14;                   // q, q_free, full/free per slot, s_full, s_free, p_ready, pv_done,
+                                             // o_free, mma_done
+
+// Ring item i of a unit, in the order the products consume the tiles: K_0, then K_{j+1} and V_j for j = 0 .. n-2,
+// then V_{n-1}.
+__device__ __forceinline__ void wide_item(int i, int n, int& which, int& tile) {
+    if (i == 0) {
+        which = 0;
+        tile = 0;
+    } else if (i == 2 * n - 1) {
+        which = 1;
+        tile = n - 1;
+    } else {
+        which = ((i - 1) & 1) ? 1 : 0;
+        tile = ((i - 1) >> 1) + (which ? 0 : 1);
+    }
+}
+
+// Named barrier 1 over the 256 softmax threads; the second form also returns whether any of them passed `flag`.
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ bool softmax_sync_any(bool flag) {
+    uint32_t any;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(any)
+        : "r"((uint32_t)flag)
+        : "memory");
+    return any != 0;
+}
+
+template <int D>
+static constexpr size_t wide_smem_bytes() {
+    // alignment slack, Q, ring, barriers, TMEM address / abort flag / armed counts, row exchange [2][128]
+    return 1024 + (size_t)(D / 64) * kRegion + (size_t)kWSlots * (D / 64) * kWRegion + 8 * kWBars + 16 + 2 * 128 * 4;
+}
+
+// A unit of prefill_wide_kernel: query tile x (counted from the last), KV head g, sequence s.  Unit w has x = w % nx:
+// the CTAs running at one time work on neighbouring query tiles of the same (sequence, KV head) and share its K and
+// V tiles in L2 (an order with the sequence fastest spread them over all rows and read K and V from DRAM once per
+// query tile), and each CTA's units (w = c + grid i) cycle through long and short query tiles alike.
+struct WideUnit {
+    int s, g, qs, q_len, tok0, ctx, pos0, ntiles;
+};
+enum { kUnitOk = 0, kUnitEmpty = 1, kUnitBadCtx = 2, kUnitOther = 3 };
+
+template <bool kBf16>
+__device__ __forceinline__ int wide_unit(const PrefillParams& p, int nx, int w, WideUnit& u) {
+    const int rest = w / nx;
+    u.tok0 = (nx - 1 - w % nx) * p.TQ;  // latest query tile first within a row
+    u.g = rest % p.H_kv;
+    u.s = rest / p.H_kv;
+    u.qs = p.q_start[u.s];
+    u.q_len = p.q_start[u.s + 1] - u.qs;
+    if (u.tok0 >= u.q_len) return kUnitEmpty;
+    u.ctx = p.ctx_lens[u.s];
+    if (u.q_len > u.ctx || u.ctx > p.MB * p.B || u.q_len < 0) return kUnitBadCtx;
+    // a bf16 row that was not staged (or that the staging marked) is prefill_kernel's, with the split P
+    if (kBf16 && (p.vstage == nullptr || p.vsplit[u.s * p.H_kv + u.g] != 0)) return kUnitOther;
+    u.pos0 = u.ctx - u.q_len + u.tok0;                              // position of the tile's first query token
+    const int nkeys = u.ctx - u.q_len + min(u.tok0 + p.TQ, u.q_len);  // keys the tile's last query sees
+    u.ntiles = (nkeys + kWKeys - 1) / kWKeys;
+    return kUnitOk;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                                     const __grid_constant__ CUtensorMap tm_kvg,
+                                                                     const __grid_constant__ CUtensorMap tm_vsg,
+                                                                     const PrefillParams p) {
+    constexpr int DH = D / 64;        // 64-column halves of a head row
+    constexpr int NK = D / 16;        // k-steps of S = Q K^T
+    constexpr int NT = kWKeys / 16;   // k-steps of O += P V
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t idesc_s = umma_idesc(kBf16, kPfRows, kWKeys, false);
+    constexpr uint32_t idesc_o = umma_idesc(false, kPfRows, D, true);
+    constexpr uint32_t kQ = DH * kRegion;      // the query tile: 128 rows x D
+    constexpr uint32_t kSlot = DH * kWRegion;  // a ring slot: 256 keys x D, [8-row group][half][8 rows][128 B]
+    constexpr uint32_t kGroup = DH * 1024;     // bytes per 8-row group of a slot
+    static_assert(wide_smem_bytes<D>() <= 232448, "shared memory");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_addr(base);
+    // Q | ring[kWSlots] | barriers
+    const uint32_t sQ = sb, sR = sQ + kQ, sBar = sR + kWSlots * kSlot;
+    const uint32_t qbar = sBar, qfree = qbar + 8, full0 = qfree + 8, free0 = full0 + 8 * kWSlots,
+                   sfull = free0 + 8 * kWSlots, sfree = sfull + 8, prdy = sfree + 8, pvd = prdy + 8, ofree = pvd + 8,
+                   mmadone = ofree + 8;
+    uint8_t* extra = base + (sBar - sb) + 8 * kWBars;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(extra);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(extra + 4);
+    volatile int* armed = abort_flag + 1;    // ring items whose copies the TMA warp has issued, for the exit path
+    volatile int* armed_q = abort_flag + 2;  // query tiles the TMA warp has loaded, likewise
+    float* xrow = reinterpret_cast<float*>(extra + 16);  // [half][row]: row maxima, at the end exponential sums
+
+    griddep_wait();
+    griddep_launch_dependents();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nx = (p.max_q_len + p.TQ - 1) / p.TQ;  // query tiles per (sequence, KV head)
+    const int n_units = nx * p.H_kv * p.N;
+    auto slot = [](int i) { return (uint32_t)(i % kWSlots); };
+    auto ph = [](int i) { return (uint32_t)((i / kWSlots) & 1); };
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid == 0) {
+        for (int i = 0; i < kWBars; ++i) mbar_init(sBar + 8 * i, 1);
+        mbar_init(sfree, kPfSoftmaxThreads);
+        mbar_init(prdy, kPfSoftmaxThreads);
+        mbar_init(ofree, kPfSoftmaxThreads);
+        *abort_flag = 0;
+        *armed = 0;
+        *armed_q = 0;
+        fence_mbar_init();
+    }
+    // rows past TQ*G (when G does not divide 128) are never loaded: clear them once
+    if (warp < 8)
+        for (int r = p.TQ * p.G + warp; r < kPfRows; r += 8)
+            for (int dh = 0; dh < DH; ++dh)
+                if (lane < 8)
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sQ + dh * kRegion + r * 128 +
+                                                                                  lane * 16),
+                                 "r"(0)
+                                 : "memory");
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;  // columns: S at 0, O at kWColO, P at kWColP
+    auto waited = [&](uint32_t bar, uint32_t parity) {
+        const bool w = mbar_wait_bounded(bar, parity, abort_flag, p.wait_ns);
+        if (!w) *abort_flag = 1;
+        return w;
+    };
+    bool ok = true;
+    WideUnit u;
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ TMA producer
+        const uint64_t pol = policy_evict_first();
+        int k = 0, item = 0;  // units and ring items of this CTA so far
+        // lane b: the physical block of the tile's b-th KV block (kept per tile parity: V_j is issued after K_{j+1})
+        int ent[2] = {0, 0};
+        for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
+            const int st = wide_unit<kBf16>(p, nx, w, u);
+            if (st == kUnitBadCtx && lane == 0) flag_error(p.err, PA_DEV_ERR_CTX);
+            if (st != kUnitOk) continue;
+            // the query buffer is free once the previous unit's last S product has completed
+            if (k > 0) ok = waited(qfree, (uint32_t)((k - 1) & 1));
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            if (lane == 0) {
+                *armed_q = k + 1;
+                mbar_arrive_expect_tx(qbar, (uint32_t)DH * p.G * p.TQ * 128);
+                for (int dh = 0; dh < DH; ++dh)
+                    tma_load_4d(sQ + dh * kRegion, &tm_q, qbar, 0, dh, u.g * p.G, u.qs + u.tok0, policy_evict_normal());
+            }
+            __syncwarp();
+            const int nitems = 2 * u.ntiles;
+            for (int i = 0; i < nitems && ok; ++i) {
+                int which, t;
+                wide_item(i, u.ntiles, which, t);
+                const int k0 = t * kWKeys;
+                const int nblk = min(kWKeys, u.ctx - k0 + p.B - 1) / p.B;  // blocks holding keys of this tile
+                if (which == 0) {
+                    int e = lane < nblk ? p.tables[(size_t)u.s * p.MB + k0 / p.B + lane] : 0;
+                    if (lane < nblk && (unsigned)e >= (unsigned)p.NB) {
+                        flag_error(p.err, PA_DEV_ERR_BLOCK);
+                        e = p.NB;  // past the tensor: TMA fills zeros
+                    }
+                    ent[t & 1] = e;
+                }
+                const int gi = item + i;
+                const uint32_t b = slot(gi);
+                // slot b is free once the products that read item gi - kWSlots have completed
+                if (gi >= kWSlots) ok = waited(free0 + 8 * b, ph(gi - kWSlots));
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                const uint32_t bar = full0 + 8 * b, dst = sR + b * kSlot;
+                if (which == 1 && kBf16) {
+                    // the staged V tile: 256 keys of this (sequence, KV head), two copies of 128 keys
+                    if (lane == 0) {
+                        *armed = gi + 1;
+                        mbar_arrive_expect_tx(bar, kSlot);
+                        for (int hh = 0; hh < 2; ++hh)
+                            tma_load_5d(dst + hh * (kSlot / 2), &tm_vsg, bar, 0, 0, 0, (k0 + hh * kPfKeys) / 8,
+                                        u.s * p.H_kv + u.g, pol);
+                    }
+                    __syncwarp();
+                    continue;
+                }
+                if (lane == 0) {
+                    *armed = gi + 1;  // expect_tx and every copy below, with no wait in between
+                    mbar_arrive_expect_tx(bar, (uint32_t)nblk * DH * p.B * 128);
+                }
+                __syncwarp();
+                const int e = ent[t & 1];
+                if (lane < nblk)
+                    tma_load_5d(dst + (uint32_t)lane * p.B * DH * 128, &tm_kvg, bar, 0, 0, 0, e * (p.B / 8),
+                                which * p.H_kv + u.g, pol);
+            }
+            item += nitems;
+            ++k;
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ MMA issuer
+        const uint64_t dq = umma_desc(sQ, 16, 1024);
+        auto issue_s = [&](int gi, bool last) {  // S = Q K^T, K (K-major, kGroup bytes per 8 rows) from ring item gi
+            const uint64_t dk = umma_desc(sR + slot(gi) * kSlot, 16, kGroup);
+#pragma unroll
+            for (int ks = 0; ks < NK; ++ks) {
+                const uint32_t qoff = (ks >> 2) * (kRegion >> 4) + (ks & 3) * 2;
+                const uint32_t koff = (ks >> 2) * (1024 >> 4) + (ks & 3) * 2;
+                umma_f16(tmem, dq + qoff, dk + koff, idesc_s, ks > 0);
+            }
+            umma_commit(sfull);
+            umma_commit(free0 + 8 * slot(gi));
+            if (last) umma_commit(qfree);  // the unit's last use of Q
+        };
+        auto issue_pv = [&](int gi, bool first) {  // O += P V, P from TMEM, V (MN-major, halves 1 KB apart) from gi
+            const uint64_t dv = umma_desc(sR + slot(gi) * kSlot, 1024, kGroup);
+#pragma unroll
+            for (int ks = 0; ks < NT; ++ks)
+                umma_f16_ta(tmem + kWColO, tmem + kWColP + ks * 8, dv + (uint64_t)(ks * ((2 * kGroup) >> 4)), idesc_o,
+                            (!first || ks > 0));
+            umma_commit(pvd);
+            umma_commit(free0 + 8 * slot(gi));
+        };
+        if (lane == 0) {
+            int k = 0, kt = 0, item = 0;  // units, key tiles and ring items of this CTA so far
+            for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
+                if (wide_unit<kBf16>(p, nx, w, u) != kUnitOk) continue;
+                const int nt = u.ntiles;
+                // S_0 overwrites the previous unit's last S once the softmax has read it, after Q and K_0 landed
+                ok = (kt == 0 || waited(sfree, (uint32_t)((kt - 1) & 1))) && waited(qbar, (uint32_t)(k & 1)) &&
+                     waited(full0 + 8 * slot(item), ph(item));
+                if (!ok) break;
+                tc_fence_after();
+                issue_s(item, nt == 1);
+                for (int j = 0; j < nt && ok; ++j) {
+                    if (j + 1 < nt) {
+                        const int ik = item + 1 + 2 * j;  // K_{j+1}: S_{j+1} overwrites S_j once the softmax read it
+                        ok = waited(sfree, (uint32_t)((kt + j) & 1)) && waited(full0 + 8 * slot(ik), ph(ik));
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(ik, j + 2 == nt);
+                    }
+                    const int iv = item + (j + 1 < nt ? 2 + 2 * j : 2 * nt - 1);  // V_j
+                    // PV_0 starts O afresh: the softmax has read the previous unit's O
+                    ok = waited(prdy, (uint32_t)((kt + j) & 1)) && (j > 0 || k == 0 ||
+                                                                   waited(ofree, (uint32_t)((k - 1) & 1))) &&
+                         waited(full0 + 8 * slot(iv), ph(iv));
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(iv, j == 0);
+                }
+                kt += nt;
+                item += 2 * nt;
+                ++k;
+            }
+            // arrives once every product issued above has completed (at once when none was issued)
+            umma_commit(mmadone);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax: thread = (query row, key half)
+        const int h = warp >> 2;               // key columns 128 h .. 128 h + 127 of every tile
+        const int r = (warp & 3) * 32 + lane;  // query row = TMEM lane
+        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t t_s = t_lane + (uint32_t)h * kPfKeys;
+        const uint32_t t_p = t_lane + kWColP + (uint32_t)h * (kPfKeys / 2);
+        const uint32_t t_o = t_lane + kWColO + (uint32_t)h * (D / 2);
+        const float NEG_INF = -INFINITY;
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        int kt = 0, item = 0;  // key tiles and ring items of this CTA so far
+        bool stop = false;
+        for (int w = blockIdx.x; w < n_units && !stop; w += gridDim.x) {
+            if (wide_unit<kBf16>(p, nx, w, u) != kUnitOk) continue;
+            const int nt = u.ntiles;
+            const int qtok = r / p.G;
+            const bool row_ok = r < p.TQ * p.G && u.tok0 + qtok < u.q_len;
+            const int qpos = row_ok ? u.pos0 + qtok : -1;  // -1 masks every key
+            float m_ref = NEG_INF, l = 0.f;
+            for (int j = 0; j < nt; ++j) {
+                const int Tj = kt + j;
+                const int k0 = j * kWKeys + h * kPfKeys;  // this half's first key
+                ok = waited(sfull, (uint32_t)(Tj & 1)) && ok;
+                tc_fence_after();
+                float v[kPfKeys];
+                {
+                    uint32_t* uu = reinterpret_cast<uint32_t*>(v);
+#pragma unroll
+                    for (int c = 0; c < kPfKeys / 32; ++c)
+                        asm volatile(
+                            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+                            "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+                            "%28, %29, %30, %31}, [%32];"
+                            : "=r"(uu[32 * c + 0]), "=r"(uu[32 * c + 1]), "=r"(uu[32 * c + 2]), "=r"(uu[32 * c + 3]),
+                              "=r"(uu[32 * c + 4]), "=r"(uu[32 * c + 5]), "=r"(uu[32 * c + 6]), "=r"(uu[32 * c + 7]),
+                              "=r"(uu[32 * c + 8]), "=r"(uu[32 * c + 9]), "=r"(uu[32 * c + 10]), "=r"(uu[32 * c + 11]),
+                              "=r"(uu[32 * c + 12]), "=r"(uu[32 * c + 13]), "=r"(uu[32 * c + 14]),
+                              "=r"(uu[32 * c + 15]), "=r"(uu[32 * c + 16]), "=r"(uu[32 * c + 17]),
+                              "=r"(uu[32 * c + 18]), "=r"(uu[32 * c + 19]), "=r"(uu[32 * c + 20]),
+                              "=r"(uu[32 * c + 21]), "=r"(uu[32 * c + 22]), "=r"(uu[32 * c + 23]),
+                              "=r"(uu[32 * c + 24]), "=r"(uu[32 * c + 25]), "=r"(uu[32 * c + 26]),
+                              "=r"(uu[32 * c + 27]), "=r"(uu[32 * c + 28]), "=r"(uu[32 * c + 29]),
+                              "=r"(uu[32 * c + 30]), "=r"(uu[32 * c + 31])
+                            : "r"(t_s + c * 32)
+                            : "memory");
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                }
+                tc_fence_before();
+                mbar_arrive(sfree);  // S is in registers: the next S product may overwrite it
+                // only tiles that reach past the query tile's first position need the causal mask
+                if (k0 + kPfKeys - 1 > u.pos0 || !row_ok) {
+#pragma unroll
+                    for (int i = 0; i < kPfKeys; ++i) v[i] = k0 + i <= qpos ? v[i] : NEG_INF;
+                }
+                float mx[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+#pragma unroll
+                for (int i = 0; i < kPfKeys; i += 8) {
+                    mx[0] = fmax3(mx[0], v[i], v[i + 1]);
+                    mx[1] = fmax3(mx[1], v[i + 2], v[i + 3]);
+                    mx[2] = fmax3(mx[2], v[i + 4], v[i + 5]);
+                    mx[3] = fmax3(mx[3], v[i + 6], v[i + 7]);
+                }
+                const float m_loc = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * p.scale_log2;  // this half's maximum
+                // One barrier per tile as a rule: it tells every softmax thread whether any wait gave up, or whether
+                // in any row either half's maximum outgrew the reference by more than 2^8.  Only then do the halves
+                // of each row exchange their maxima through shared memory (a second barrier, which carries the abort
+                // too: every softmax thread leaves at the same barrier).  Otherwise both halves keep the reference,
+                // as the exchange would have decided.
+                float m_tile = m_loc;
+                if (softmax_sync_any(j == 0 || m_loc > m_ref + 8.f || !ok || *abort_flag)) {
+                    xrow[h * kPfRows + r] = m_loc;
+                    if (softmax_sync_any(!ok || *abort_flag)) {
+                        ok = false;
+                        stop = true;
+                        break;
+                    }
+                    m_tile = fmaxf(xrow[r], xrow[kPfRows + r]);
+                }
+                // both halves of a row take the same decisions from the same values
+                float m_new = m_ref;
+                if (j == 0 || m_tile > m_ref + 8.f) m_new = fmaxf(m_ref, m_tile);
+                const float alpha = (j == 0 || m_new == m_ref) ? 1.f : fast_exp2(m_ref - m_new);
+                m_ref = m_new;
+                const float m_use = m_new == NEG_INF ? 0.f : m_new;
+                const float2 nm2 = make_float2(-m_use, -m_use);
+                float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                uint32_t pk[kPfKeys / 2];
+#pragma unroll
+                for (int i = 0; i < kPfKeys; i += 2) {
+                    float2 x = ffma2(make_float2(v[i], v[i + 1]), sc2, nm2);
+                    x.x = fast_exp2(x.x);
+                    x.y = fast_exp2(x.y);
+                    ls[(i >> 1) & 1] = fadd2(ls[(i >> 1) & 1], x);
+                    pk[i / 2] = Mma<__half>::pack(x.x, x.y);
+                }
+                const float2 lsum = fadd2(ls[0], ls[1]);
+                l = fmaf(l, alpha, lsum.x + lsum.y);
+                // P takes the previous P's columns, and a rescale of O must see the previous PV: both wait for it
+                if (Tj > 0) {
+                    ok = waited(pvd, (uint32_t)((Tj - 1) & 1)) && ok;
+                    tc_fence_after();
+                    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                        for (int c = 0; c < D / 64; ++c) {
+                            float o[32];
+                            tmem_ld32(t_o + c * 32, o);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                            tmem_st32(t_o + c * 32, o);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < kPfKeys / 32; ++c) {
+                    uint32_t w16[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) w16[i] = pk[16 * c + i];
+                    tmem_st16(t_p + c * 16, w16);
+                }
+                // V rows past the context may hold anything (even NaN) in a tile read from the pool: they are zeroed
+                // before PV meets them with P = 0 (a staged tile has zeros there already)
+                const int nvalid = min(kWKeys, u.ctx - j * kWKeys);
+                if (nvalid < kWKeys && !kBf16) {
+                    const int iv = item + (j + 1 < nt ? 2 + 2 * j : 2 * nt - 1);
+                    ok = waited(full0 + 8 * slot(iv), ph(iv)) && ok;
+                    const uint32_t vb = sR + slot(iv) * kSlot;
+                    for (int rr = nvalid + warp; rr < kWKeys; rr += 8)
+                        for (int dh = 0; dh < DH; ++dh)
+                            if (lane < 8)
+                                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
+                                                 vb + (uint32_t)(rr >> 3) * kGroup + dh * 1024 + (rr & 7) * 128 +
+                                                 lane * 16),
+                                             "r"(0)
+                                             : "memory");
+                }
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(prdy);
+            }
+            if (stop) break;
+            // the row's exponential sum: this half's plus the other's
+            softmax_sync();
+            xrow[h * kPfRows + r] = l;
+            softmax_sync();
+            const float l_row = xrow[r] + xrow[kPfRows + r];
+            if (ok) ok = waited(pvd, (uint32_t)((kt + nt - 1) & 1));
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                tc_fence_after();
+                const float inv = 1.f / l_row;
+                const size_t orow =
+                    ((size_t)(u.qs + u.tok0 + qtok) * p.H_q + (size_t)u.g * p.G + (r % p.G)) * D + h * (D / 2);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    float o[32];
+                    tmem_ld32(t_o + c * 32, o);
+                    if (c == D / 64 - 1) {
+                        tc_fence_before();
+                        mbar_arrive(ofree);  // O is read: the next unit's first value product may start it afresh
+                    }
+                    if (!row_ok) continue;
+                    if (p.out_dtype == PA_F32) {
+                        // 256-bit stores: each lane writes whole 32-byte sectors of its row (the host checks that
+                        // `out` is 32-byte aligned; rows are D floats long)
+                        float* dst = static_cast<float*>(p.out) + orow + c * 32;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 8 * i),
+                                         "f"(o[8 * i] * inv), "f"(o[8 * i + 1] * inv), "f"(o[8 * i + 2] * inv),
+                                         "f"(o[8 * i + 3] * inv), "f"(o[8 * i + 4] * inv), "f"(o[8 * i + 5] * inv),
+                                         "f"(o[8 * i + 6] * inv), "f"(o[8 * i + 7] * inv)
+                                         : "memory");
+                    } else {
+                        T* dst = static_cast<T*>(p.out) + orow + c * 32;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) dst[i] = from_float<T>(o[i] * inv);
+                    }
+                }
+            } else {
+                mbar_arrive(ofree);
+            }
+            kt += nt;
+            item += 2 * nt;
+        }
+    }
+    // Nothing issued may still be running when TMEM and shared memory are released: the products (the MMA
+    // thread's last commit) and the copies (the last query tile loaded, each loaded after the previous one was used;
+    // and the last arm of each ring slot: slot b's arms are items b, b + 3, ..., each consumed before the next was
+    // armed, so only the last can be in flight).
+    if (warp == 9 && lane == 0) mbar_wait_bounded(mmadone, 0, nullptr);
+    if (warp == 8 && lane == 0) {
+        const int nq = *armed_q;
+        if (nq > 0) mbar_wait_bounded(qbar, (uint32_t)((nq - 1) & 1), nullptr);
+        const int n = *armed;
+        for (int b = 0; b < kWSlots && b < n; ++b)
+            mbar_wait_bounded(full0 + 8 * b, ph(b + (n - 1 - b) / kWSlots * kWSlots), nullptr);
+    }
+    tc_fence_before();
+    ok = __syncthreads_and(ok && !*abort_flag);
+    if (!ok && tid == 0) flag_error(p.err, PA_DEV_ERR_TIMEOUT);
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
 // ----------------------------------------------------------------------------- host
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -739,6 +1247,12 @@ static EncodeTiledFn pf_encode_fn() {
     return fn;
 }
 
+// PA_PREFILL_KERNEL=narrow: every row through prefill_kernel (two 128-row query tiles per CTA, 128-key tiles)
+static bool prefill_narrow_forced() {
+    const char* v = std::getenv("PA_PREFILL_KERNEL");
+    return v != nullptr && std::strcmp(v, "narrow") == 0;
+}
+
 static size_t prefill_smem_bytes(int D) {
     const int DH = D / 64;
     return 1024 + (size_t)(2 + 2 * kPfStages) * DH * kRegion + 256;  // Q[2], K[NS], V[NS], barriers
@@ -747,7 +1261,7 @@ static size_t prefill_smem_bytes(int D) {
 bool prefill_workspace_layout(int N, int H_kv, int D, int B, int MB, PrefillWorkspace* L) {
     if (N <= 0 || H_kv <= 0 || (D != 64 && D != 128) || B <= 0 || MB <= 0) return false;
     const long long keys = (long long)MB * B;
-    L->S_pad = (int)((keys + kPfKeys - 1) / kPfKeys * kPfKeys);
+    L->S_pad = (int)((keys + kStagePad - 1) / kStagePad * kStagePad);
     const size_t stage = (size_t)N * H_kv * L->S_pad * D * 2;
     L->split = (stage + 255) & ~size_t(255);
     L->total = L->split + (((size_t)N * H_kv * sizeof(int) + 255) & ~size_t(255));
@@ -757,7 +1271,7 @@ bool prefill_workspace_layout(int N, int H_kv, int D, int B, int MB, PrefillWork
 template <typename T, int D>
 static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tkv,
                              const CUtensorMap& tkv_blk, const CUtensorMap& tvs, const CUtensorMap* tvall,
-                             const PrefillWorkspace* ws) {
+                             const CUtensorMap* tkvg, const CUtensorMap* tvsg, const PrefillWorkspace* ws) {
     auto kern = prefill_kernel<T, D>;
     const size_t smem = prefill_smem_bytes(D);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -783,6 +1297,8 @@ static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const 
     int* vsplit = ws ? reinterpret_cast<int*>(static_cast<uint8_t*>(a.workspace) + ws->split) : nullptr;
     p.vsplit = vsplit;
     p.S_pad = ws ? ws->S_pad : 0;
+    p.only_split = 0;
+    p.max_q_len = a.max_q_len;
     p.err = a.dev_err;
     if (ws) {
         // stage V as fp16 (before the prefill kernel, same stream); the rows it marks start unmarked
@@ -798,6 +1314,27 @@ static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const 
                           p.wait_ns, a.dev_err);
         count_launch();
         if (e != cudaSuccess) return cuda_fail(e, "V staging launch");
+    }
+    // fp16 caches and staged bf16 rows: prefill_wide_kernel (fp16 P); bf16 rows without staging, or marked by it:
+    // prefill_kernel with the split P (launched after the wide kernel, it serves only the marked rows)
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    if ((!kBf16 || ws) && !prefill_narrow_forced()) {
+        auto wide = prefill_wide_kernel<T, D>;
+        constexpr size_t wsmem = wide_smem_bytes<D>();
+        e = cudaFuncSetAttribute(wide, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsmem);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill wide)");
+        // persistent: one CTA per SM (the shared memory allows no second), at most one per unit
+        const long long units = (long long)((a.max_q_len + p.TQ - 1) / p.TQ) * a.H_kv * a.N;
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+            sms = 1;
+        const dim3 wgrid((unsigned)std::min<long long>(units, sms));
+        e = launch_kernel(wide, wgrid, dim3(kPfThreads), wsmem, a.stream, tq, *tkvg, *tvsg, p);
+        count_launch();
+        if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+        if (!kBf16) return PA_OK;
+        p.only_split = 1;
     }
     const dim3 grid((a.max_q_len + 2 * p.TQ - 1) / (2 * p.TQ), a.H_kv, a.N);
     e = launch_kernel(kern, grid, dim3(kPfThreads), smem, a.stream, tq, tkv, tkv_blk, tvs, p);
@@ -865,12 +1402,38 @@ pa_status launch_prefill(const PrefillArgs& a) {
         if (r != CUDA_SUCCESS)
             return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(pool V rows) failed (CUresult %d)", (int)r);
     }
+    // prefill_wide_kernel's views: a slot holds [8-row group][column half][8 rows][64 columns].  The pool: dims 64
+    // columns, token within a group of 8, column half, group of 8 tokens (over all blocks), K/V x kv head; box = one
+    // block.  The staged V: dims 64 columns, key within a group, column half, group of 8 keys, (sequence, kv head);
+    // box = 128 keys.
+    CUtensorMap tkvg, tvsg;
+    std::memset(&tkvg, 0, sizeof tkvg);
+    std::memset(&tvsg, 0, sizeof tvsg);
+    {
+        cuuint64_t gd[5] = {64, 8, (cuuint64_t)DH, (cuuint64_t)a.NB * a.B / 8, (cuuint64_t)2 * a.H_kv};
+        cuuint64_t gs[4] = {(cuuint64_t)2 * a.H_kv * a.D * 2, 128, (cuuint64_t)8 * 2 * a.H_kv * a.D * 2,
+                            (cuuint64_t)a.D * 2};
+        cuuint32_t gb[5] = {64, 8, (cuuint32_t)DH, (cuuint32_t)(a.B / 8), 1};
+        r = fn(&tkvg, dt, 5, const_cast<void*>(a.pool), gd, gs, gb, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(pool groups) failed (CUresult %d)", (int)r);
+    }
+    if (use_ws) {
+        cuuint64_t vd[5] = {64, 8, (cuuint64_t)DH, (cuuint64_t)ws.S_pad / 8, (cuuint64_t)a.N * a.H_kv};
+        cuuint64_t vs[4] = {(cuuint64_t)a.D * 2, 128, (cuuint64_t)8 * a.D * 2, (cuuint64_t)ws.S_pad * a.D * 2};
+        cuuint32_t vb[5] = {64, 8, (cuuint32_t)DH, (cuuint32_t)(kPfKeys / 8), 1};
+        r = fn(&tvsg, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5, a.workspace, vd, vs, vb, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(staged V groups) failed (CUresult %d)", (int)r);
+    }
     const PrefillWorkspace* w = use_ws ? &ws : nullptr;
     if (a.kv_dtype == PA_BF16)
-        return a.D == 128 ? run_prefill<__nv_bfloat16, 128>(a, tq, tkv, tkv_blk, tvs, &tvall, w)
-                          : run_prefill<__nv_bfloat16, 64>(a, tq, tkv, tkv_blk, tvs, &tvall, w);
-    return a.D == 128 ? run_prefill<__half, 128>(a, tq, tkv, tkv_blk, tvs, &tvall, w)
-                      : run_prefill<__half, 64>(a, tq, tkv, tkv_blk, tvs, &tvall, w);
+        return a.D == 128 ? run_prefill<__nv_bfloat16, 128>(a, tq, tkv, tkv_blk, tvs, &tvall, &tkvg, &tvsg, w)
+                          : run_prefill<__nv_bfloat16, 64>(a, tq, tkv, tkv_blk, tvs, &tvall, &tkvg, &tvsg, w);
+    return a.D == 128 ? run_prefill<__half, 128>(a, tq, tkv, tkv_blk, tvs, &tvall, &tkvg, &tvsg, w)
+                      : run_prefill<__half, 64>(a, tq, tkv, tkv_blk, tvs, &tvall, &tkvg, &tvsg, w);
 }
 
 }  // namespace pa

@@ -33,9 +33,20 @@ def _with_ctx(w, ctx):
     return w
 
 
+def _kernel(monkeypatch, kernel):
+    """Selects the prefill kernel of the call: "wide" (one query tile per CTA, 256-key tiles; the default for fp16
+    caches and staged bf16 rows) or "narrow" (two query tiles per CTA, 128-key tiles, for every row)."""
+    if kernel == "narrow":
+        monkeypatch.setenv("PA_PREFILL_KERNEL", "narrow")
+    else:
+        monkeypatch.delenv("PA_PREFILL_KERNEL", raising=False)
+
+
+@pytest.mark.parametrize("kernel", ["wide", "narrow"])
 @pytest.mark.parametrize("stage_v", [True, False], ids=["staged_v", "split_p"])
 @pytest.mark.parametrize("chunks_of", ["full", "tail", "mixed"])
-def test_prefill_llama_shaped_every_output(chunks_of, stage_v):
+def test_prefill_llama_shaped_every_output(chunks_of, stage_v, kernel, monkeypatch):
+    _kernel(monkeypatch, kernel)
     w = _with_ctx(W.llama3_8b(n_seqs=4), [200, 513, 77, 1000])
     c = C.build_paged(w)
     chunks = {"full": list(w.ctx), "tail": [1, 1, 1, 1], "mixed": [200, 130, 1, 257]}[chunks_of]
@@ -49,14 +60,18 @@ def test_prefill_llama_shaped_every_output(chunks_of, stage_v):
     (lambda: W.yi34b_long(n_seqs=2, ctx_len=600, B=8), [600, 331], [600, 200]),   # G = 7, B = 8
     (lambda: W.yi34b_long(n_seqs=2, ctx_len=600, B=32), [600, 331], [333, 331]),  # B = 32
 ])
-def test_prefill_group_sizes_and_block_sizes(make, ctx, chunks, stage_v):
+@pytest.mark.parametrize("kernel", ["wide", "narrow"])
+def test_prefill_group_sizes_and_block_sizes(make, ctx, chunks, stage_v, kernel, monkeypatch):
+    _kernel(monkeypatch, kernel)
     c = C.build_paged(_with_ctx(make(), ctx))
     out, ref, _, _ = _run(c, chunks, stage_v=stage_v)
     C.assert_close(out.cpu().numpy(), ref, f"prefill {c.w.name}")
 
 
+@pytest.mark.parametrize("kernel", ["wide", "narrow"])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_prefill_head_dim_64(dtype):
+def test_prefill_head_dim_64(dtype, kernel, monkeypatch):
+    _kernel(monkeypatch, kernel)
     w = W.Workload("d64", 1, 3, 8, 2, 64, 8, dtype, np.array([100, 9, 256], np.int32), 200,
                    np.random.default_rng(3).permutation(200).astype(np.int32))
     c = C.build_paged(w)
