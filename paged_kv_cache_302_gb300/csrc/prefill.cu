@@ -895,7 +895,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __gri
 
     if (warp == 8) {
         // ------------------------------------------------------------ TMA producer
-        const uint64_t pol = policy_evict_first();
+        // K and V of a (sequence, KV head) serve every query tile of the row, which neighbouring CTAs run at the
+        // same time: kept in L2 (evict_last); a query tile is read once (evict_first)
+        const uint64_t pol = policy_evict_last();
         int k = 0, item = 0;  // units and ring items of this CTA so far
         // lane b: the physical block of the tile's b-th KV block (kept per tile parity: V_j is issued after K_{j+1})
         int ent[2] = {0, 0};
@@ -911,7 +913,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __gri
                 *armed_q = k + 1;
                 mbar_arrive_expect_tx(qbar, (uint32_t)DH * p.G * p.TQ * 128);
                 for (int dh = 0; dh < DH; ++dh)
-                    tma_load_4d(sQ + dh * kRegion, &tm_q, qbar, 0, dh, u.g * p.G, u.qs + u.tok0, policy_evict_normal());
+                    tma_load_4d(sQ + dh * kRegion, &tm_q, qbar, 0, dh, u.g * p.G, u.qs + u.tok0, policy_evict_first());
             }
             __syncwarp();
             const int nitems = 2 * u.ntiles;
@@ -1247,10 +1249,16 @@ static EncodeTiledFn pf_encode_fn() {
     return fn;
 }
 
-// PA_PREFILL_KERNEL=narrow: every row through prefill_kernel (two 128-row query tiles per CTA, 128-key tiles)
-static bool prefill_narrow_forced() {
+// Which kernel serves the rows with an fp16 value product.  prefill_wide_kernel loads its K and V tiles one KV
+// block per copy for one query tile; prefill_kernel shares each copy between two query tiles.  With 8-token blocks
+// the wide kernel's copies are 2 KB and four times as many per FLOP, and it measured slower (fp16 819 against 1125
+// TFLOP/s, bf16 staged 1029 against 1066); from 16 tokens it is as fast or faster (fp16 1128 / 1286 against 1110 /
+// 1128 at B = 16 / 32, bf16 staged 1193 / 1234 against 1046 / 1047).  PA_PREFILL_KERNEL=narrow or =wide forces one.
+static bool prefill_use_wide(int B) {
     const char* v = std::getenv("PA_PREFILL_KERNEL");
-    return v != nullptr && std::strcmp(v, "narrow") == 0;
+    if (v != nullptr && std::strcmp(v, "narrow") == 0) return false;
+    if (v != nullptr && std::strcmp(v, "wide") == 0) return true;
+    return B >= 16;
 }
 
 static size_t prefill_smem_bytes(int D) {
@@ -1315,10 +1323,11 @@ static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const 
         count_launch();
         if (e != cudaSuccess) return cuda_fail(e, "V staging launch");
     }
-    // fp16 caches and staged bf16 rows: prefill_wide_kernel (fp16 P); bf16 rows without staging, or marked by it:
-    // prefill_kernel with the split P (launched after the wide kernel, it serves only the marked rows)
+    // fp16 caches and staged bf16 rows: prefill_wide_kernel (fp16 P) from 16-token blocks; bf16 rows without staging,
+    // or marked by it: prefill_kernel with the split P (launched after the wide kernel, it serves only the marked
+    // rows); everything else: prefill_kernel
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-    if ((!kBf16 || ws) && !prefill_narrow_forced()) {
+    if ((!kBf16 || ws) && prefill_use_wide(a.B)) {
         auto wide = prefill_wide_kernel<T, D>;
         constexpr size_t wsmem = wide_smem_bytes<D>();
         e = cudaFuncSetAttribute(wide, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsmem);

@@ -34,12 +34,10 @@ def _with_ctx(w, ctx):
 
 
 def _kernel(monkeypatch, kernel):
-    """Selects the prefill kernel of the call: "wide" (one query tile per CTA, 256-key tiles; the default for fp16
-    caches and staged bf16 rows) or "narrow" (two query tiles per CTA, 128-key tiles, for every row)."""
-    if kernel == "narrow":
-        monkeypatch.setenv("PA_PREFILL_KERNEL", "narrow")
-    else:
-        monkeypatch.delenv("PA_PREFILL_KERNEL", raising=False)
+    """Forces the prefill kernel of the call: "wide" (persistent, one query tile per unit, 256-key tiles; by default
+    used for fp16 caches and staged bf16 rows from 16-token blocks) or "narrow" (two query tiles per CTA, 128-key
+    tiles, for every row)."""
+    monkeypatch.setenv("PA_PREFILL_KERNEL", kernel)
 
 
 @pytest.mark.parametrize("kernel", ["wide", "narrow"])
