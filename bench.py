@@ -735,7 +735,13 @@ def measure_prefill(steps: int = 10, warmup: int = 3) -> list:
         # the fp16 dense tensor rate equals the bf16 one on this GPU
         how = ("V staged as fp16 by a first kernel (included), one value product" if stage_v and name == "bf16"
                else "P split into two bf16 parts, two value products" if name == "bf16" else "fp16 P, one product")
-        res.append({"kv_dtype": name, "value_product": how, "unit": "TFLOP/s", "value": tf, "ms_per_call": t * 1e3,
+        # the library's choice of kernel for these rows (prefill.cu: the wide kernel serves fp16 value products from
+        # 16-token blocks; PA_PREFILL_KERNEL forces one)
+        force = os.environ.get("PA_PREFILL_KERNEL", "")
+        wide = (name == "f16" or stage_v) and (force == "wide" or (force != "narrow" and B >= 16))
+        kernel = "prefill_wide_kernel" if wide else "prefill_kernel"
+        res.append({"kv_dtype": name, "value_product": how, "kernel": kernel, "unit": "TFLOP/s", "value": tf,
+                    "ms_per_call": t * 1e3,
                     "peak_bf16_tflops": peak, "peak_source": peak_src, "frac": tf / peak, "seqs": N, "ctx": ctx_len,
                     "chunk": chunk, "flops_per_call": flops, "calls": steps})
         del pool, q
