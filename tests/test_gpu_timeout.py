@@ -91,7 +91,9 @@ def test_contiguous_decode_timeout_exit():
     assert err.item() == 0 and torch.equal(again, clean)
 
 
-def test_prefill_timeout_exit_flags_returns_and_leaves_the_gpu_usable():
+@pytest.mark.parametrize("kernel", ["wide", "narrow"])
+def test_prefill_timeout_exit_flags_returns_and_leaves_the_gpu_usable(kernel, monkeypatch):
+    monkeypatch.setenv("PA_PREFILL_KERNEL", kernel)  # each prefill kernel through its exit path
     w = W.llama3_8b(n_seqs=3, grow=1024)
     w.ctx = np.asarray([1500, 700, 1024], dtype=np.int32)
     c = C.build_paged(w, check_pool=False)
