@@ -771,14 +771,15 @@ __device__ __forceinline__ void wide_item(int i, int n, int& which, int& tile) {
     }
 }
 
-// Named barrier 1 over the 256 softmax threads; the second form also returns whether any of them passed `flag`.
-__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-__device__ __forceinline__ bool softmax_sync_any(bool flag) {
+// Named barrier `id` over the 64 threads of the two softmax warps that hold the same query rows (warps w and
+// w + 4, ids 1-4); the second form also returns whether any of them passed `flag`.
+__device__ __forceinline__ void pair_sync(uint32_t id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
+__device__ __forceinline__ bool pair_sync_any(uint32_t id, bool flag) {
     uint32_t any;
     asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %2, 0;\n\tbar.red.or.pred q, %1, 64, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(any)
-        : "r"((uint32_t)flag)
+        : "r"(id), "r"((uint32_t)flag)
         : "memory");
     return any != 0;
 }
@@ -1026,6 +1027,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __gri
         // ------------------------------------------------------------ softmax: thread = (query row, key half)
         const int h = warp >> 2;               // key columns 128 h .. 128 h + 127 of every tile
         const int r = (warp & 3) * 32 + lane;  // query row = TMEM lane
+        const uint32_t pair = 1 + (warp & 3);  // named barrier of the two warps holding rows r
         const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t t_s = t_lane + (uint32_t)h * kPfKeys;
         const uint32_t t_p = t_lane + kWColP + (uint32_t)h * (kPfKeys / 2);
@@ -1085,15 +1087,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __gri
                     mx[3] = fmax3(mx[3], v[i + 6], v[i + 7]);
                 }
                 const float m_loc = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * p.scale_log2;  // this half's maximum
-                // One barrier per tile as a rule: it tells every softmax thread whether any wait gave up, or whether
-                // in any row either half's maximum outgrew the reference by more than 2^8.  Only then do the halves
-                // of each row exchange their maxima through shared memory (a second barrier, which carries the abort
-                // too: every softmax thread leaves at the same barrier).  Otherwise both halves keep the reference,
-                // as the exchange would have decided.
+                // One barrier per tile as a rule, between the two warps of these rows: it tells both whether a wait
+                // gave up, or whether in any of their rows either half's maximum outgrew the reference by more than
+                // 2^8.  Only then do the halves of each row exchange their maxima through shared memory (a second
+                // barrier, which carries the abort too: the pair leaves at the same barrier, and the other pairs
+                // find the abort flag at their next wait).  Otherwise both halves keep the reference, as the
+                // exchange would have decided.
                 float m_tile = m_loc;
-                if (softmax_sync_any(j == 0 || m_loc > m_ref + 8.f || !ok || *abort_flag)) {
+                if (pair_sync_any(pair, j == 0 || m_loc > m_ref + 8.f || !ok || *abort_flag)) {
                     xrow[h * kPfRows + r] = m_loc;
-                    if (softmax_sync_any(!ok || *abort_flag)) {
+                    if (pair_sync_any(pair, !ok || *abort_flag)) {
                         ok = false;
                         stop = true;
                         break;
@@ -1164,9 +1167,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __gri
             }
             if (stop) break;
             // the row's exponential sum: this half's plus the other's
-            softmax_sync();
+            pair_sync(pair);
             xrow[h * kPfRows + r] = l;
-            softmax_sync();
+            pair_sync(pair);
             const float l_row = xrow[r] + xrow[kPfRows + r];
             if (ok) ok = waited(pvd, (uint32_t)((kt + nt - 1) & 1));
             ok = __all_sync(0xffffffffu, ok);
