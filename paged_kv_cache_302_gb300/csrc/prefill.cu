@@ -113,6 +113,37 @@ __device__ __forceinline__ void umma_commit(uint32_t mbar) {
                  : "memory");
 }
 
+// Arrives on the mbarrier at this offset in every CTA of the cluster named by `mask` once the products issued so
+// far have completed.
+__device__ __forceinline__ void umma_commit_mc(uint32_t mbar, uint16_t mask) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+                     "r"(mbar),
+                 "h"(mask)
+                 : "memory");
+}
+
+// 5-D tiled load multicast to the same shared-memory offset of every CTA of the cluster in `mask`; each destination
+// CTA's mbarrier at offset `bar` counts the bytes it receives.
+__device__ __forceinline__ void tma_load_5d_mc(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1, int c2,
+                                               int c3, int c4, uint16_t mask, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8, %9;" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar), "h"(mask), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of both CTAs of the cluster: writes before it are visible to the other CTA after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -790,36 +821,43 @@ static constexpr size_t wide_smem_bytes() {
     return 1024 + (size_t)(D / 64) * kRegion + (size_t)kWSlots * (D / 64) * kWRegion + 8 * kWBars + 16 + 2 * 128 * 4;
 }
 
-// A unit of prefill_wide_kernel: query tile x (counted from the last), KV head g, sequence s.  Unit w has x = w % nx:
-// the CTAs running at one time work on neighbouring query tiles of the same (sequence, KV head) and share its K and
-// V tiles in L2 (an order with the sequence fastest spread them over all rows and read K and V from DRAM once per
-// query tile), and each CTA's units (w = c + grid i) cycle through long and short query tiles alike.
+// A unit of prefill_wide_kernel is a pair of neighbouring query tiles of one (sequence, KV head), one per CTA of a
+// cluster: pair px (counted from the last) holds query tiles x = 2 px (rank 0, the later one: the most keys) and
+// 2 px + 1 (rank 1).  Unit w has px = w % npx: the clusters running at one time work on neighbouring pairs of the
+// same row and share its K and V in L2 (an order with the sequence fastest read K and V from DRAM once per query
+// tile), and each cluster's units (w = c + clusters i) cycle through long and short query tiles alike.  Both CTAs
+// load the pair's key tiles (as many as rank 0's rows need); rank 1's keys past its own causal range are masked.
+// A CTA whose tile holds no row of the chunk (rank 0's past its end, or rank 1's at tok0 < 0 when the row has an
+// odd number of query tiles) still takes its part in the copies and computes no row.
 struct WideUnit {
     int s, g, qs, q_len, tok0, ctx, pos0, ntiles;
 };
 enum { kUnitOk = 0, kUnitEmpty = 1, kUnitBadCtx = 2, kUnitOther = 3 };
 
 template <bool kBf16>
-__device__ __forceinline__ int wide_unit(const PrefillParams& p, int nx, int w, WideUnit& u) {
-    const int rest = w / nx;
-    u.tok0 = (nx - 1 - w % nx) * p.TQ;  // latest query tile first within a row
+__device__ __forceinline__ int wide_unit(const PrefillParams& p, int nx, int npx, int w, int rank, WideUnit& u) {
+    const int rest = w / npx;
+    const int tok_pair = (nx - 1 - 2 * (w % npx)) * p.TQ;  // rank 0's first query token
     u.g = rest % p.H_kv;
     u.s = rest / p.H_kv;
     u.qs = p.q_start[u.s];
     u.q_len = p.q_start[u.s + 1] - u.qs;
-    if (u.tok0 >= u.q_len) return kUnitEmpty;
+    // empty when both tiles lie past the chunk (rank 1's, the earlier one, included); rank 0's tile alone may
+    if (u.q_len <= 0 || tok_pair - p.TQ >= u.q_len) return kUnitEmpty;
     u.ctx = p.ctx_lens[u.s];
     if (u.q_len > u.ctx || u.ctx > p.MB * p.B || u.q_len < 0) return kUnitBadCtx;
     // a bf16 row that was not staged (or that the staging marked) is prefill_kernel's, with the split P
     if (kBf16 && (p.vstage == nullptr || p.vsplit[u.s * p.H_kv + u.g] != 0)) return kUnitOther;
-    u.pos0 = u.ctx - u.q_len + u.tok0;                              // position of the tile's first query token
-    const int nkeys = u.ctx - u.q_len + min(u.tok0 + p.TQ, u.q_len);  // keys the tile's last query sees
+    u.tok0 = tok_pair - rank * p.TQ;                                  // this CTA's query tile
+    u.pos0 = u.ctx - u.q_len + u.tok0;                                // position of its first query token
+    const int nkeys = u.ctx - u.q_len + min(tok_pair + p.TQ, u.q_len);  // keys the pair's last query sees
     u.ntiles = (nkeys + kWKeys - 1) / kWKeys;
     return kUnitOk;
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q,
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPfThreads, 1)
+    prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                      const __grid_constant__ CUtensorMap tm_kvg,
                                                                      const __grid_constant__ CUtensorMap tm_vsg,
                                                                      const PrefillParams p) {
@@ -852,7 +890,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __gri
     griddep_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nx = (p.max_q_len + p.TQ - 1) / p.TQ;  // query tiles per (sequence, KV head)
-    const int n_units = nx * p.H_kv * p.N;
+    const int npx = (nx + 1) / 2;                     // pairs of them
+    const int n_units = npx * p.H_kv * p.N;
+    const int rank = (int)cluster_rank();
+    const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;  // this cluster, clusters
     auto slot = [](int i) { return (uint32_t)(i % kWSlots); };
     auto ph = [](int i) { return (uint32_t)((i / kWSlots) & 1); };
 
@@ -864,6 +905,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __gri
     }
     if (tid == 0) {
         for (int i = 0; i < kWBars; ++i) mbar_init(sBar + 8 * i, 1);
+        for (int b = 0; b < kWSlots; ++b) mbar_init(free0 + 8 * b, 2);  // a slot is free once both CTAs used it
         mbar_init(sfree, kPfSoftmaxThreads);
         mbar_init(prdy, kPfSoftmaxThreads);
         mbar_init(ofree, kPfSoftmaxThreads);
@@ -885,6 +927,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __gri
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    cluster_sync();  // both CTAs' barriers are initialised before either copies or signals into the other
     const uint32_t tmem = *tmem_slot;  // columns: S at 0, O at kWColO, P at kWColP
     auto waited = [&](uint32_t bar, uint32_t parity) {
         const bool w = mbar_wait_bounded(bar, parity, abort_flag, p.wait_ns);
@@ -902,8 +945,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __gri
         int k = 0, item = 0;  // units and ring items of this CTA so far
         // lane b: the physical block of the tile's b-th KV block (kept per tile parity: V_j is issued after K_{j+1})
         int ent[2] = {0, 0};
-        for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
-            const int st = wide_unit<kBf16>(p, nx, w, u);
+        for (int w = cid; w < n_units && ok; w += ncl) {
+            const int st = wide_unit<kBf16>(p, nx, npx, w, rank, u);
             if (st == kUnitBadCtx && lane == 0) flag_error(p.err, PA_DEV_ERR_CTX);
             if (st != kUnitOk) continue;
             // the query buffer is free once the previous unit's last S product has completed
@@ -933,19 +976,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __gri
                 }
                 const int gi = item + i;
                 const uint32_t b = slot(gi);
-                // slot b is free once the products that read item gi - kWSlots have completed
+                // slot b is free once the products of both CTAs that read item gi - kWSlots have completed (either
+                // CTA's copies write the slot in both)
                 if (gi >= kWSlots) ok = waited(free0 + 8 * b, ph(gi - kWSlots));
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 const uint32_t bar = full0 + 8 * b, dst = sR + b * kSlot;
+                // Each CTA copies half of the tile into both CTAs' slot (multicast) and expects the whole tile's bytes
+                // on its own barrier; the other half may land before this CTA arms it (the phase cannot complete
+                // before the arrival below).
                 if (which == 1 && kBf16) {
-                    // the staged V tile: 256 keys of this (sequence, KV head), two copies of 128 keys
+                    // the staged V tile: 256 keys of this (sequence, KV head); rank r copies keys 128 r .. + 127
                     if (lane == 0) {
                         *armed = gi + 1;
                         mbar_arrive_expect_tx(bar, kSlot);
-                        for (int hh = 0; hh < 2; ++hh)
-                            tma_load_5d(dst + hh * (kSlot / 2), &tm_vsg, bar, 0, 0, 0, (k0 + hh * kPfKeys) / 8,
-                                        u.s * p.H_kv + u.g, pol);
+                        tma_load_5d_mc(dst + (uint32_t)rank * (kSlot / 2), &tm_vsg, bar, 0, 0, 0,
+                                       (k0 + rank * kPfKeys) / 8, u.s * p.H_kv + u.g, 0x3, pol);
                     }
                     __syncwarp();
                     continue;
@@ -956,9 +1002,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __gri
                 }
                 __syncwarp();
                 const int e = ent[t & 1];
-                if (lane < nblk)
-                    tma_load_5d(dst + (uint32_t)lane * p.B * DH * 128, &tm_kvg, bar, 0, 0, 0, e * (p.B / 8),
-                                which * p.H_kv + u.g, pol);
+                if (lane < nblk && (lane & 1) == rank)  // rank r copies the blocks b = r (mod 2)
+                    tma_load_5d_mc(dst + (uint32_t)lane * p.B * DH * 128, &tm_kvg, bar, 0, 0, 0, e * (p.B / 8),
+                                   which * p.H_kv + u.g, 0x3, pol);
             }
             item += nitems;
             ++k;
@@ -975,8 +1021,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __gri
                 umma_f16(tmem, dq + qoff, dk + koff, idesc_s, ks > 0);
             }
             umma_commit(sfull);
-            umma_commit(free0 + 8 * slot(gi));
-            if (last) umma_commit(qfree);  // the unit's last use of Q
+            umma_commit_mc(free0 + 8 * slot(gi), 0x3);  // both CTAs' slot: either may copy the next item into it
+            if (last) umma_commit(qfree);              // the unit's last use of Q
         };
         auto issue_pv = [&](int gi, bool first) {  // O += P V, P from TMEM, V (MN-major, halves 1 KB apart) from gi
             const uint64_t dv = umma_desc(sR + slot(gi) * kSlot, 1024, kGroup);
@@ -985,12 +1031,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __gri
                 umma_f16_ta(tmem + kWColO, tmem + kWColP + ks * 8, dv + (uint64_t)(ks * ((2 * kGroup) >> 4)), idesc_o,
                             (!first || ks > 0));
             umma_commit(pvd);
-            umma_commit(free0 + 8 * slot(gi));
+            umma_commit_mc(free0 + 8 * slot(gi), 0x3);
         };
         if (lane == 0) {
             int k = 0, kt = 0, item = 0;  // units, key tiles and ring items of this CTA so far
-            for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
-                if (wide_unit<kBf16>(p, nx, w, u) != kUnitOk) continue;
+            for (int w = cid; w < n_units && ok; w += ncl) {
+                if (wide_unit<kBf16>(p, nx, npx, w, rank, u) != kUnitOk) continue;
                 const int nt = u.ntiles;
                 // S_0 overwrites the previous unit's last S once the softmax has read it, after Q and K_0 landed
                 ok = (kt == 0 || waited(sfree, (uint32_t)((kt - 1) & 1))) && waited(qbar, (uint32_t)(k & 1)) &&
@@ -1036,11 +1082,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __gri
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
         int kt = 0, item = 0;  // key tiles and ring items of this CTA so far
         bool stop = false;
-        for (int w = blockIdx.x; w < n_units && !stop; w += gridDim.x) {
-            if (wide_unit<kBf16>(p, nx, w, u) != kUnitOk) continue;
+        for (int w = cid; w < n_units && !stop; w += ncl) {
+            if (wide_unit<kBf16>(p, nx, npx, w, rank, u) != kUnitOk) continue;
             const int nt = u.ntiles;
             const int qtok = r / p.G;
-            const bool row_ok = r < p.TQ * p.G && u.tok0 + qtok < u.q_len;
+            const bool row_ok = r < p.TQ * p.G && u.tok0 >= 0 && u.tok0 + qtok < u.q_len;
             const int qpos = row_ok ? u.pos0 + qtok : -1;  // -1 masks every key
             float m_ref = NEG_INF, l = 0.f;
             for (int j = 0; j < nt; ++j) {
@@ -1212,9 +1258,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __gri
         }
     }
     // Nothing issued may still be running when TMEM and shared memory are released: the products (the MMA
-    // thread's last commit) and the copies (the last query tile loaded, each loaded after the previous one was used;
-    // and the last arm of each ring slot: slot b's arms are items b, b + 3, ..., each consumed before the next was
-    // armed, so only the last can be in flight).
+    // thread's last commit, which follows its commits into the other CTA's barriers) and the copies (the last query
+    // tile loaded, each loaded after the previous one was used; and the last arm of each ring slot: slot b's arms
+    // are items b, b + 3, ..., each consumed before the next was armed, so only the last can be in flight; its
+    // phase completes once both CTAs' halves have landed).  Then the cluster barrier: neither CTA leaves while the
+    // other may still copy or signal into it.
     if (warp == 9 && lane == 0) mbar_wait_bounded(mmadone, 0, nullptr);
     if (warp == 8 && lane == 0) {
         const int nq = *armed_q;
@@ -1226,6 +1274,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_wide_kernel(const __gri
     tc_fence_before();
     ok = __syncthreads_and(ok && !*abort_flag);
     if (!ok && tid == 0) flag_error(p.err, PA_DEV_ERR_TIMEOUT);
+    cluster_sync();
     if (warp == 0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
@@ -1335,13 +1384,25 @@ static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const 
         constexpr size_t wsmem = wide_smem_bytes<D>();
         e = cudaFuncSetAttribute(wide, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsmem);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill wide)");
-        // persistent: one CTA per SM (the shared memory allows no second), at most one per unit
-        const long long units = (long long)((a.max_q_len + p.TQ - 1) / p.TQ) * a.H_kv * a.N;
-        int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
-            sms = 1;
-        const dim3 wgrid((unsigned)std::min<long long>(units, sms));
+        // persistent: as many 2-CTA clusters as fit at once (one CTA per SM: the shared memory allows no second),
+        // at most one per unit (pair of query tiles)
+        static int max_clusters[64] = {0};  // per device, per instantiation
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+        if (max_clusters[dev] == 0) {
+            cudaLaunchConfig_t occ = {};
+            occ.gridDim = dim3(2);
+            occ.blockDim = dim3(kPfThreads);
+            occ.dynamicSmemBytes = wsmem;
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, wide, &occ);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters(prefill wide)");
+            max_clusters[dev] = n > 0 ? n : -1;
+        }
+        if (max_clusters[dev] < 0) return fail(PA_ERR_UNSUPPORTED, "prefill: no 2-CTA cluster fits on this device");
+        const int nx = (a.max_q_len + p.TQ - 1) / p.TQ;
+        const long long units = (long long)((nx + 1) / 2) * a.H_kv * a.N;
+        const dim3 wgrid((unsigned)(2 * std::min<long long>(units, max_clusters[dev])));
         e = launch_kernel(wide, wgrid, dim3(kPfThreads), wsmem, a.stream, tq, *tkvg, *tvsg, p);
         count_launch();
         if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
