@@ -735,10 +735,9 @@ def measure_prefill(steps: int = 10, warmup: int = 3) -> list:
         # the fp16 dense tensor rate equals the bf16 one on this GPU
         how = ("V staged as fp16 by a first kernel (included), one value product" if stage_v and name == "bf16"
                else "P split into two bf16 parts, two value products" if name == "bf16" else "fp16 P, one product")
-        # the library's choice of kernel for these rows (prefill.cu: the wide kernel serves fp16 value products from
-        # 16-token blocks; PA_PREFILL_KERNEL forces one)
-        force = os.environ.get("PA_PREFILL_KERNEL", "")
-        wide = (name == "f16" or stage_v) and (force == "wide" or (force != "narrow" and B >= 16))
+        # the library's choice of kernel for these rows (prefill.cu: the wide kernel serves fp16 value products;
+        # PA_PREFILL_KERNEL=narrow forces the two-tile kernel)
+        wide = (name == "f16" or stage_v) and os.environ.get("PA_PREFILL_KERNEL", "") != "narrow"
         kernel = "prefill_wide_kernel" if wide else "prefill_kernel"
         res.append({"kv_dtype": name, "value_product": how, "kernel": kernel, "unit": "TFLOP/s", "value": tf,
                     "ms_per_call": t * 1e3,

@@ -215,9 +215,9 @@ pa_status pa_decode_contiguous(void* out, pa_dtype out_dtype, const void* q, con
  * the same precision).  fp16 caches ignore the workspace.  The workspace's
  * contents need not be initialised; calls that overlap on the GPU must not
  * share one.  Rows with an fp16 value product run on a persistent kernel
- * over 256-key tiles when B >= 16, the others on a kernel with two query
- * tiles per CTA; the environment variable PA_PREFILL_KERNEL=wide or =narrow
- * forces one of the two (results differ only by rounding order).
+ * over 256-key tiles (2-CTA clusters), the others on a kernel with two query
+ * tiles per CTA; the environment variable PA_PREFILL_KERNEL=narrow puts
+ * every row on the second (results differ only by rounding order).
  * Supported: kv_dtype F16/BF16, D in {64, 128}, B in {8, 16, 32},
  * H_q / H_kv <= 128, N <= 65535, scale > 0.  out, q, pool and workspace must
  * be 16-byte aligned, an fp32 out 32-byte aligned (PA_ERR_INVALID otherwise).

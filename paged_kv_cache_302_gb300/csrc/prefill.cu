@@ -1301,16 +1301,13 @@ static EncodeTiledFn pf_encode_fn() {
     return fn;
 }
 
-// Which kernel serves the rows with an fp16 value product.  prefill_wide_kernel loads its K and V tiles one KV
-// block per copy for one query tile; prefill_kernel shares each copy between two query tiles.  With 8-token blocks
-// the wide kernel's copies are 2 KB and four times as many per FLOP, and it measured slower (fp16 819 against 1125
-// TFLOP/s, bf16 staged 1029 against 1066); from 16 tokens it is as fast or faster (fp16 1128 / 1286 against 1110 /
-// 1128 at B = 16 / 32, bf16 staged 1193 / 1234 against 1046 / 1047).  PA_PREFILL_KERNEL=narrow or =wide forces one.
-static bool prefill_use_wide(int B) {
+// Which kernel serves the rows with an fp16 value product: prefill_wide_kernel, unless PA_PREFILL_KERNEL=narrow
+// (prefill_kernel for every row; =wide names the default).  Measured on the same FLOPs (fp16 / bf16 with V staged,
+// TFLOP/s): B = 8: 1122 / 1228 against 1120 / 1064; B = 16: 1335 / 1256 against 1122 / 1048; B = 32: 1314 / 1263
+// against 1107 / 1070.  Before its clusters shared each copy, the wide kernel lost at B = 8 (fp16 819).
+static bool prefill_use_wide() {
     const char* v = std::getenv("PA_PREFILL_KERNEL");
-    if (v != nullptr && std::strcmp(v, "narrow") == 0) return false;
-    if (v != nullptr && std::strcmp(v, "wide") == 0) return true;
-    return B >= 16;
+    return !(v != nullptr && std::strcmp(v, "narrow") == 0);
 }
 
 static size_t prefill_smem_bytes(int D) {
@@ -1375,11 +1372,10 @@ static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const 
         count_launch();
         if (e != cudaSuccess) return cuda_fail(e, "V staging launch");
     }
-    // fp16 caches and staged bf16 rows: prefill_wide_kernel (fp16 P) from 16-token blocks; bf16 rows without staging,
-    // or marked by it: prefill_kernel with the split P (launched after the wide kernel, it serves only the marked
-    // rows); everything else: prefill_kernel
+    // fp16 caches and staged bf16 rows: prefill_wide_kernel (fp16 P); bf16 rows without staging, or marked by it:
+    // prefill_kernel with the split P (launched after the wide kernel, it serves only the marked rows)
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-    if ((!kBf16 || ws) && prefill_use_wide(a.B)) {
+    if ((!kBf16 || ws) && prefill_use_wide()) {
         auto wide = prefill_wide_kernel<T, D>;
         constexpr size_t wsmem = wide_smem_bytes<D>();
         e = cudaFuncSetAttribute(wide, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsmem);

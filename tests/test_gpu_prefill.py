@@ -34,9 +34,9 @@ def _with_ctx(w, ctx):
 
 
 def _kernel(monkeypatch, kernel):
-    """Forces the prefill kernel of the call: "wide" (persistent, one query tile per unit, 256-key tiles; by default
-    used for fp16 caches and staged bf16 rows from 16-token blocks) or "narrow" (two query tiles per CTA, 128-key
-    tiles, for every row)."""
+    """Selects the prefill kernel of the call: "wide" (the default: persistent 2-CTA clusters, one query tile per
+    CTA, 256-key tiles, for fp16 caches and staged bf16 rows) or "narrow" (two query tiles per CTA, 128-key tiles,
+    for every row)."""
     monkeypatch.setenv("PA_PREFILL_KERNEL", kernel)
 
 
