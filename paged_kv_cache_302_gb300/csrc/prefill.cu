@@ -760,24 +760,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 // ----------------------------------------------------------------------------- one query tile, 256-key tiles
 
 // prefill_wide_kernel: the same computation for the rows whose value product takes P in fp16 (an fp16 cache, or a
-// bf16 cache's rows that stage_v_kernel converted; the rows it marked are left to prefill_kernel).  A unit of work
-// is one 128-row query tile of one (sequence, KV head).  S = Q K^T of 256 keys at once: a tcgen05.mma of N = 256 per
+// bf16 cache's rows that stage_v_kernel converted; the rows it marked are left to prefill_kernel).  A CTA works on
+// one 128-row query tile of one (sequence, KV head) at a time.  S = Q K^T of 256 keys at once: a tcgen05.mma of N = 256 per
 // 16 columns of the head dim runs the tensor core at its full rate, where N = 128 products chained into one
 // accumulator (prefill_kernel's) ran at ~60 % of it.  S sits in TMEM columns [0, 256) and P (fp16) in columns of
 // its own, [384, 512), so the S product of the next key tile is issued as soon as the softmax has read S into
 // registers and runs while the exponentials are computed; O += P V (16 keys per product, O in columns
 // [256, 256 + D)) follows once P is written.
-// The kernel is persistent: one CTA per SM takes units c, c + grid, c + 2 grid, ... (ordered as wide_unit states),
-// so the set-up (TMEM, barriers) is paid once.  Between units the next query tile is loaded while the softmax works on the
-// last key tile, and the next unit's first S product runs while the softmax writes out the last unit's O.
-// Barrier phases follow counters that run across units (units, key tiles, ring items of the CTA).
+// The kernel is persistent and runs as clusters of two CTAs, one CTA per SM: cluster c takes units c, c + clusters,
+// ... (ordered as wide_unit states), a unit being two neighbouring query tiles, one per CTA.  Both CTAs need the same
+// K and V tiles: each copies half of every tile's blocks into both CTAs' shared memory (TMA multicast), which halves
+// the copies and the L2 reads per SM.  The set-up (TMEM, barriers) is paid once.  Between units the next query tile
+// is loaded while the softmax works on the last key tile.  Barrier phases follow counters that run across units
+// (units, key tiles, ring items).
 //   * warps 0-7 (softmax): warp w owns TMEM lanes 32 (w % 4) .. + 31 (query rows) and key columns 128 (w / 4) ..
 //     + 127 of each tile; the two warps of a row share their row maxima through shared memory when either grew, so
 //     both halves of P have one scale, and at the end their exponential sums; each stores D / 2 columns of O;
 //   * warp 8 (TMA): Q, then the K and V tiles into a ring of three 256-key slots in the order the products consume
 //     them (per unit: K_0, then K_{j+1}, V_j, ..., then the last V).  A slot is laid out [8-row group][column half]
 //     [8 rows][128 B], so one copy brings a whole KV block (both column halves of its B rows): lane b issues the
-//     copy of the tile's b-th block; a staged V tile is two copies of 128 keys;
+//     copy of the tile's b-th block when b has this CTA's parity; a staged V tile is two copies of 128 keys, one
+//     per CTA.  A slot is free again once both CTAs' products have read it;
 //   * warp 9 (MMA, one thread): per unit S_0, then S_{j+1} once the softmax has read S_j and PV_j once P_j is
 //     written.
 constexpr int kWSlots = 3;                   // ring slots, each one 256-key K or V tile
