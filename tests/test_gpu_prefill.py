@@ -209,3 +209,21 @@ def test_prefill_bf16_staging_head_groups(H_q, H_kv):
     for stage_v in (True, False):
         out, ref, _, _ = _run(c, [700, 100, 333], stage_v=stage_v)
         C.assert_close(out.cpu().numpy(), ref, f"prefill H_kv={H_kv} stage_v={stage_v}")
+
+
+@pytest.mark.parametrize("kernel", ["wide", "narrow"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("G", [16, 40, 128])
+def test_prefill_large_head_groups(G, dtype, kernel, monkeypatch):
+    """Many query heads per KV head: a 128-row query tile holds 128/G tokens (8, 3 and 1; with G = 40 eight rows
+    of each tile are unused), so a chunk spans many query tiles and pairs of them.  Every output against the
+    oracle, each prefill kernel in turn."""
+    _kernel(monkeypatch, kernel)
+    H_kv = 2 if G < 128 else 1
+    ctx = np.array([300, 45], dtype=np.int32)
+    NB = int(sum(-(-ctx // 16))) + 8
+    w = W.Workload(f"group{G}", 21, 2, G * H_kv, H_kv, 128, 16, dtype, ctx, NB,
+                   np.random.default_rng(21).permutation(NB).astype(np.int32))
+    c = C.build_paged(w)
+    out, ref, _, _ = _run(c, [300, 7])
+    C.assert_close(out.cpu().numpy(), ref, f"prefill G={G} {dtype} {kernel}")
