@@ -946,8 +946,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPfThreads, 1)
         // same time: kept in L2 (evict_last); a query tile is read once (evict_first)
         const uint64_t pol = policy_evict_last();
         int k = 0, item = 0;  // units and ring items of this CTA so far
-        // lane b: the physical block of the tile's b-th KV block (kept per tile parity: V_j is issued after K_{j+1})
-        int ent[2] = {0, 0};
+        // lane b: the physical block of the tile's b-th KV block, kept per tile parity (V_j is issued after K_{j+1})
+        // in two registers
+        int ent_even = 0, ent_odd = 0;
         for (int w = cid; w < n_units && ok; w += ncl) {
             const int st = wide_unit<kBf16>(p, nx, npx, w, rank, u);
             if (st == kUnitBadCtx && lane == 0) flag_error(p.err, PA_DEV_ERR_CTX);
@@ -975,7 +976,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPfThreads, 1)
                         flag_error(p.err, PA_DEV_ERR_BLOCK);
                         e = p.NB;  // past the tensor: TMA fills zeros
                     }
-                    ent[t & 1] = e;
+                    if (t & 1)
+                        ent_odd = e;
+                    else
+                        ent_even = e;
                 }
                 const int gi = item + i;
                 const uint32_t b = slot(gi);
@@ -1004,7 +1008,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPfThreads, 1)
                     mbar_arrive_expect_tx(bar, (uint32_t)nblk * DH * p.B * 128);
                 }
                 __syncwarp();
-                const int e = ent[t & 1];
+                const int e = (t & 1) ? ent_odd : ent_even;
                 if (lane < nblk && (lane & 1) == rank)  // rank r copies the blocks b = r (mod 2)
                     tma_load_5d_mc(dst + (uint32_t)lane * p.B * DH * 128, &tm_kvg, bar, 0, 0, 0, e * (p.B / 8),
                                    which * p.H_kv + u.g, 0x3, pol);
