@@ -32,6 +32,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -1389,10 +1390,11 @@ static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const 
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill wide)");
         // persistent: as many 2-CTA clusters as fit at once (one CTA per SM: the shared memory allows no second),
         // at most one per unit (pair of query tiles)
-        static int max_clusters[64] = {0};  // per device, per instantiation
+        static std::atomic<int> max_clusters[64];  // per device, per instantiation; 0 = not yet asked
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-        if (max_clusters[dev] == 0) {
+        int ncl = max_clusters[dev].load(std::memory_order_relaxed);
+        if (ncl == 0) {
             cudaLaunchConfig_t occ = {};
             occ.gridDim = dim3(2);
             occ.blockDim = dim3(kPfThreads);
@@ -1400,17 +1402,19 @@ static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const 
             int n = 0;
             e = cudaOccupancyMaxActiveClusters(&n, wide, &occ);
             if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters(prefill wide)");
-            max_clusters[dev] = n > 0 ? n : -1;
+            ncl = n > 0 ? n : -1;
+            max_clusters[dev].store(ncl, std::memory_order_relaxed);
         }
-        if (max_clusters[dev] < 0) return fail(PA_ERR_UNSUPPORTED, "prefill: no 2-CTA cluster fits on this device");
-        const int nx = (a.max_q_len + p.TQ - 1) / p.TQ;
-        const long long units = (long long)((nx + 1) / 2) * a.H_kv * a.N;
-        const dim3 wgrid((unsigned)(2 * std::min<long long>(units, max_clusters[dev])));
-        e = launch_kernel(wide, wgrid, dim3(kPfThreads), wsmem, a.stream, tq, *tkvg, *tvsg, p);
-        count_launch();
-        if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
-        if (!kBf16) return PA_OK;
-        p.only_split = 1;
+        if (ncl > 0) {  // otherwise (no 2-CTA cluster fits) every row goes to prefill_kernel below
+            const int nx = (a.max_q_len + p.TQ - 1) / p.TQ;
+            const long long units = (long long)((nx + 1) / 2) * a.H_kv * a.N;
+            const dim3 wgrid((unsigned)(2 * std::min<long long>(units, ncl)));
+            e = launch_kernel(wide, wgrid, dim3(kPfThreads), wsmem, a.stream, tq, *tkvg, *tvsg, p);
+            count_launch();
+            if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+            if (!kBf16) return PA_OK;
+            p.only_split = 1;
+        }
     }
     const dim3 grid((a.max_q_len + 2 * p.TQ - 1) / (2 * p.TQ), a.H_kv, a.N);
     e = launch_kernel(kern, grid, dim3(kPfThreads), smem, a.stream, tq, tkv, tkv_blk, tvs, p);
