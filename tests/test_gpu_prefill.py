@@ -227,3 +227,26 @@ def test_prefill_large_head_groups(G, dtype, kernel, monkeypatch):
     c = C.build_paged(w)
     out, ref, _, _ = _run(c, [300, 7])
     C.assert_close(out.cpu().numpy(), ref, f"prefill G={G} {dtype} {kernel}")
+
+
+@pytest.mark.parametrize("kernel", ["wide", "narrow"])
+def test_prefill_empty_chunks_and_a_generous_max_q_len(kernel, monkeypatch):
+    """Sequences with no chunk rows between others, and max_q_len well above the longest chunk: the units past every
+    chunk are empty and write nothing; every row of the chunks against the oracle, and no row outside them is
+    touched (the output starts as NaN)."""
+    _kernel(monkeypatch, kernel)
+    w = _with_ctx(W.llama3_8b(n_seqs=4), [300, 77, 129, 513])
+    c = C.build_paged(w)
+    chunks = [0, 77, 0, 300]
+    q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    T = int(q_start[-1])
+    q = W.normal_bits(np.random.default_rng(4), (T, w.H_q, w.D), w.dtype)
+    tab, ctx = c.dev_tables()
+    out = torch.full((T + 8, w.H_q, w.D), float("nan"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_prefill(out[:T], C.to_dev(q, w.dtype), c.pool, tab, ctx, torch.from_numpy(q_start).cuda(), 1000, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    ref = oracle.paged_prefill(q, c.host_pool, c.tables, c.ctx, q_start, w.dtype, nthreads=0)
+    C.assert_close(out[:T].cpu().numpy(), ref, f"prefill empty chunks {kernel}")
+    assert torch.isnan(out[T:]).all(), "rows past the chunks were written"
