@@ -981,8 +981,8 @@ static cudaError_t reduce_dispatch_d(void* out, const float* m2, const float* l,
     const dim3 block(kReduceWarps * 32);
     if (P >= kWideMergeParts) {
         if (D == 128)
-            return launch_kernel(partition_reduce_wide_kernel<OutT, 128>, dim3(R), block, 0, st, static_cast<OutT*>(out),
-                                 m2, l, acc, nparts, rows_per_seq, R, P, skip ? 1 : 0, err);
+            return launch_kernel(partition_reduce_wide_kernel<OutT, 128>, dim3(R), block, 0, st,
+                                 static_cast<OutT*>(out), m2, l, acc, nparts, rows_per_seq, R, P, skip ? 1 : 0, err);
         return launch_kernel(partition_reduce_wide_kernel<OutT, 64>, dim3(R), block, 0, st, static_cast<OutT*>(out), m2,
                              l, acc, nparts, rows_per_seq, R, P, skip ? 1 : 0, err);
     }

@@ -762,9 +762,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 
 // prefill_wide_kernel: the same computation for the rows whose value product takes P in fp16 (an fp16 cache, or a
 // bf16 cache's rows that stage_v_kernel converted; the rows it marked are left to prefill_kernel).  A CTA works on
-// one 128-row query tile of one (sequence, KV head) at a time.  S = Q K^T of 256 keys at once: a tcgen05.mma of N = 256 per
-// 16 columns of the head dim runs the tensor core at its full rate, where N = 128 products chained into one
-// accumulator (prefill_kernel's) ran at ~60 % of it.  S sits in TMEM columns [0, 256) and P (fp16) in columns of
+// one 128-row query tile of one (sequence, KV head) at a time.  S = Q K^T of 256 keys at once: a tcgen05.mma of
+// N = 256 per 16 columns of the head dim runs the tensor core at its full rate, where N = 128 products chained into
+// one accumulator (prefill_kernel's) ran at ~60 % of it.  S sits in TMEM columns [0, 256) and P (fp16) in columns of
 // its own, [384, 512), so the S product of the next key tile is issued as soon as the softmax has read S into
 // registers and runs while the exponentials are computed; O += P V (16 keys per product, O in columns
 // [256, 256 + D)) follows once P is written.
