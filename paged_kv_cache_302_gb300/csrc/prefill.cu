@@ -1405,9 +1405,10 @@ static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const 
             ncl = n > 0 ? n : -1;
             max_clusters[dev].store(ncl, std::memory_order_relaxed);
         }
-        if (ncl > 0) {  // otherwise (no 2-CTA cluster fits) every row goes to prefill_kernel below
-            const int nx = (a.max_q_len + p.TQ - 1) / p.TQ;
-            const long long units = (long long)((nx + 1) / 2) * a.H_kv * a.N;
+        const long long nx = ((long long)a.max_q_len + p.TQ - 1) / p.TQ;
+        const long long units = (nx + 1) / 2 * a.H_kv * a.N;  // the kernel counts units in int
+        // otherwise (no 2-CTA cluster fits, or more units than an int counts) every row goes to prefill_kernel
+        if (ncl > 0 && units < (1LL << 31)) {
             const dim3 wgrid((unsigned)(2 * std::min<long long>(units, ncl)));
             e = launch_kernel(wide, wgrid, dim3(kPfThreads), wsmem, a.stream, tq, *tkvg, *tvsg, p);
             count_launch();
