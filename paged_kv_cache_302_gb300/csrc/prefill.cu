@@ -1399,10 +1399,15 @@ static pa_status run_prefill(const PrefillArgs& a, const CUtensorMap& tq, const 
             occ.gridDim = dim3(2);
             occ.blockDim = dim3(kPfThreads);
             occ.dynamicSmemBytes = wsmem;
-            int n = 0;
+            int n = 0, per_sm = 0;
             e = cudaOccupancyMaxActiveClusters(&n, wide, &occ);
             if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters(prefill wide)");
-            ncl = n > 0 ? n : -1;
+            // Each CTA allocates all 512 TMEM columns and keeps them for the whole (persistent) kernel: a second CTA
+            // on the same SM would wait in tcgen05.alloc, and with cluster partners waiting on each other that can
+            // close a cycle.  Registers (320 threads x 168) allow one CTA per SM; anything else is not launched.
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, wide, kPfThreads, wsmem);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(prefill wide)");
+            ncl = (n > 0 && per_sm == 1) ? n : -1;
             max_clusters[dev].store(ncl, std::memory_order_relaxed);
         }
         const long long nx = ((long long)a.max_q_len + p.TQ - 1) / p.TQ;
