@@ -861,10 +861,8 @@ __device__ __forceinline__ int wide_unit(const PrefillParams& p, int nx, int npx
 
 template <typename T, int D>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPfThreads, 1)
-    prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q,
-                                                                     const __grid_constant__ CUtensorMap tm_kvg,
-                                                                     const __grid_constant__ CUtensorMap tm_vsg,
-                                                                     const PrefillParams p) {
+    prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kvg,
+                        const __grid_constant__ CUtensorMap tm_vsg, const PrefillParams p) {
     constexpr int DH = D / 64;        // 64-column halves of a head row
     constexpr int NK = D / 16;        // k-steps of S = Q K^T
     constexpr int NT = kWKeys / 16;   // k-steps of O += P V
