@@ -686,19 +686,16 @@ def run_swap(args):
 
 
 def measure_prefill(steps: int = 10, warmup: int = 3) -> list:
-    """Chunked paged prefill on the tensor cores: Llama-3-8B shapes (32 q / 8 KV heads, D 128, B 16), 16 sequences
-    whose last 2048 of 4096 tokens are the chunk (K/V already in the pool); bf16, then the same shapes in fp16
-    (whose probabilities need one value product instead of two).  FLOPs count the causal score and value
-    products actually needed: 4 * D * (position + 1) per query row and head.  Calls back to back, CUDA events."""
+    """Chunked paged prefill on the tensor cores: Llama-3-8B shapes (32 q / 8 KV heads, D 128), 16 sequences whose
+    last 2048 of 4096 tokens are the chunk (K/V already in the pool).  With 16-token blocks: bf16 with V staged,
+    bf16 without a workspace (split P) and fp16; then bf16 staged and fp16 with 8- and 32-token blocks.  FLOPs
+    count the causal score and value products actually needed: 4 * D * (position + 1) per query row and head.
+    Calls back to back, CUDA events."""
     import torch
 
     import paged_kv_cache_302_gb300 as pa
 
-    N, ctx_len, chunk, H_q, H_kv, D, B = 16, 4096, 2048, 32, 8, 128, 16
-    nb = ctx_len // B
-    NB = N * nb + 64
-    perm = torch.from_numpy(np.random.default_rng(13).permutation(NB)[: N * nb].astype(np.int32))
-    tables = perm.view(N, nb).cuda()
+    N, ctx_len, chunk, H_q, H_kv, D = 16, 4096, 2048, 32, 8, 128
     ctx = torch.full((N,), ctx_len, dtype=torch.int32, device="cuda")
     q_start = torch.arange(0, (N + 1) * chunk, chunk, dtype=torch.int32, device="cuda")
     out = torch.empty((N * chunk, H_q, D), dtype=torch.float32, device="cuda")
@@ -711,26 +708,33 @@ def measure_prefill(steps: int = 10, warmup: int = 3) -> list:
         peak_src = "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"
     except Exception:
         pass
-    ws = torch.empty(pa.pa_prefill_workspace_bytes(N, H_kv, D, B, nb), dtype=torch.uint8, device="cuda")
     res = []
-    for dt, name, stage_v in ((torch.bfloat16, "bf16", True), (torch.bfloat16, "bf16", False),
-                              (torch.float16, "f16", False)):
+    cases = [(16, torch.bfloat16, "bf16", True), (16, torch.bfloat16, "bf16", False), (16, torch.float16, "f16", False),
+             (8, torch.bfloat16, "bf16", True), (8, torch.float16, "f16", False),
+             (32, torch.bfloat16, "bf16", True), (32, torch.float16, "f16", False)]
+    for B, dt, name, stage_v in cases:
+        nb = ctx_len // B
+        NB = N * nb + 64
+        perm = torch.from_numpy(np.random.default_rng(13).permutation(NB)[: N * nb].astype(np.int32))
+        tables = perm.view(N, nb).cuda()
+        ws = torch.empty(pa.pa_prefill_workspace_bytes(N, H_kv, D, B, nb), dtype=torch.uint8, device="cuda")
         pool = torch.empty((NB, B, 2, H_kv, D), dtype=dt, device="cuda").normal_()
         q = torch.empty((N * chunk, H_q, D), dtype=dt, device="cuda").normal_()
 
         def call():
             pa.pa_prefill(out, q, pool, tables, ctx, q_start, chunk, workspace=ws, stage_v=stage_v, dev_err=err)
 
+        n = steps if B == 16 else max(3, steps // 2)
         for _ in range(warmup):
             call()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for _ in range(steps):
+        for _ in range(n):
             call()
         e1.record()
         torch.cuda.synchronize()
         assert int(err.item()) == 0
-        t = e0.elapsed_time(e1) * 1e-3 / steps
+        t = e0.elapsed_time(e1) * 1e-3 / n
         tf = flops / t / 1e12
         # the fp16 dense tensor rate equals the bf16 one on this GPU
         how = ("V staged as fp16 by a first kernel (included), one value product" if stage_v and name == "bf16"
@@ -739,11 +743,11 @@ def measure_prefill(steps: int = 10, warmup: int = 3) -> list:
         # PA_PREFILL_KERNEL=narrow forces the two-tile kernel)
         wide = (name == "f16" or stage_v) and os.environ.get("PA_PREFILL_KERNEL", "") != "narrow"
         kernel = "prefill_wide_kernel" if wide else "prefill_kernel"
-        res.append({"kv_dtype": name, "value_product": how, "kernel": kernel, "unit": "TFLOP/s", "value": tf,
-                    "ms_per_call": t * 1e3,
-                    "peak_bf16_tflops": peak, "peak_source": peak_src, "frac": tf / peak, "seqs": N, "ctx": ctx_len,
-                    "chunk": chunk, "flops_per_call": flops, "calls": steps})
-        del pool, q
+        res.append({"kv_dtype": name, "block_tokens": B, "value_product": how, "kernel": kernel, "unit": "TFLOP/s",
+                    "value": tf, "ms_per_call": t * 1e3, "peak_bf16_tflops": peak, "peak_source": peak_src,
+                    "frac": tf / peak, "seqs": N, "ctx": ctx_len, "chunk": chunk, "flops_per_call": flops,
+                    "calls": n})
+        del pool, q, ws
     return res
 
 
