@@ -4,7 +4,8 @@ Each case draws its shape from a seeded generator -- query heads per KV head G i
 block size 4..32, fp16 or bf16, a partition length, 1-9 sequences with lengths from 1 to a few thousand --
 builds the pool through the C++ allocator and pa_reshape_and_cache (bit-exact against the oracle's cache
 write), and compares every output row of the paged decode, of the contiguous decode over the same K/V, and of
-the prefill over random chunks (bf16 both with V staged and with the split P), element by element.
+the prefill over random chunks (bf16 both with V staged and with the split P; every fourth shape on the
+two-tile prefill kernel), element by element.
 """
 import numpy as np
 import pytest
@@ -64,8 +65,10 @@ def test_decode_sweep_paged_and_contiguous_every_output(seed):
     C.assert_close(out2.cpu().numpy(), ref2, f"{w.name} contiguous")
 
 
-@pytest.mark.parametrize("seed", range(24))
-def test_prefill_sweep_every_output(seed):
+@pytest.mark.parametrize("seed", range(40))
+def test_prefill_sweep_every_output(seed, monkeypatch):
+    # every fourth shape on the two-tile kernel, the rest on the default (persistent 2-CTA clusters)
+    monkeypatch.setenv("PA_PREFILL_KERNEL", "narrow" if seed % 4 == 3 else "wide")
     w = _random_workload(seed, prefill=True)
     c = C.build_paged(w)
     rng = np.random.default_rng(seed + 7)
