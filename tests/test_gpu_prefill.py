@@ -250,3 +250,33 @@ def test_prefill_empty_chunks_and_a_generous_max_q_len(kernel, monkeypatch):
     ref = oracle.paged_prefill(q, c.host_pool, c.tables, c.ctx, q_start, w.dtype, nthreads=0)
     C.assert_close(out[:T].cpu().numpy(), ref, f"prefill empty chunks {kernel}")
     assert torch.isnan(out[T:]).all(), "rows past the chunks were written"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_prefill_repeated_calls_are_bit_identical(dtype):
+    """The persistent 2-CTA kernel's copies, shared free barriers and exit ordering, exercised 200 times back to
+    back: every call bit-identical to the first, no device flags.  Chunks of 1000, 37 and 7 tokens give rows with
+    an odd number of query tiles (a pair whose second CTA has no rows) and rows far shorter than the longest."""
+    w = _with_ctx(W.llama3_8b(n_seqs=3), [1500, 300, 7])
+    if dtype == "f16":
+        w.dtype = "f16"
+    c = C.build_paged(w)
+    chunks = [1000, 37, 7]
+    q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    T = int(q_start[-1])
+    q = C.to_dev(W.normal_bits(np.random.default_rng(9), (T, w.H_q, w.D), w.dtype), w.dtype)
+    tab, ctx = c.dev_tables()
+    qs = torch.from_numpy(q_start).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    first = torch.full((T, w.H_q, w.D), float("nan"), device="cuda")
+    pa.pa_prefill(first, q, c.pool, tab, ctx, qs, max(chunks), dev_err=err)
+    outs = [torch.full_like(first, float("nan")) for _ in range(4)]
+    same = torch.ones(1, dtype=torch.bool, device="cuda")
+    for i in range(200):
+        o = outs[i % 4]
+        pa.pa_prefill(o, q, c.pool, tab, ctx, qs, max(chunks), dev_err=err)
+        same &= (o == first).all()  # on the device: no synchronisation inside the loop
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert bool(same.item()), "a repeated prefill differs from the first call"
+    assert np.all(np.isfinite(first.cpu().numpy()))
